@@ -1,0 +1,331 @@
+#!/usr/bin/env python3
+"""Benchmark: fused ring all-reduce-average, N=8 workers x P=300M fp32.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one ra_allreduce_avg over the 8 workers' 1.2 GB fp32 gradient
+arrays (the 300M-parameter speech model of Gibiansky, "The Communication
+Problem"), inputs resident in HBM.  The metric is HBM GB/s over the minimum
+traffic of the all-reduce, 2*N*P*4 bytes per step (every input read once,
+the mean written to every worker once).  One JSON line is printed by rank 0.
+
+--gpus N > 1 runs under torchrun as N independent replicas (the path has no
+exchange between GPUs: all workers live in one GPU's memory); value sums the
+replicas' bytes over the slowest replica's time.
+
+--impl reference times the CPU oracle (a literal, single-threaded
+simulation of the ring) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "all-reduce-avg HBM GB/s and % of GB300 peak at N=8, P=300M fp32"
+WORKLOAD = "speech300m_n8_f32"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+CPU_SAMPLE_P = 25_000_000  # elements per worker in the oracle's bounded sample
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class _ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        loaded = [x for x in sm if smax and x >= 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+def _source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "gradient_ring_all_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profile(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("source_hash") == _source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def _cpu_oracle_sample(n: int, p: int, reps: int):
+    """Time the oracle (as it stands) on a bounded sample: a ring of n workers
+    x p elements of the workload's distribution.  Returns (GB/s, seconds)."""
+    import oracle
+    import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    rows = [synth.normal_f32(wl.seed, k, wl.scale, 0, p) for k in range(n)]
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.ring_allreduce_avg_f32(rows)
+    dt = time.perf_counter() - t0
+    return 2.0 * n * p * 4 * reps / dt / 1e9, dt
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    import synth
+    oracle.build()
+    synth.build()
+    wl = synth.WORKLOADS[WORKLOAD]
+    # per-step sample sized so that all W + K steps take about a minute
+    # (one 25M-element step is about 0.6 s of one core)
+    p = int(min(CPU_SAMPLE_P, max(1_000_000, CPU_SAMPLE_P * 100 // (args.steps + args.warmup))))
+    rows = [synth.normal_f32(wl.seed, k, wl.scale, 0, p) for k in range(wl.n)]
+    for _ in range(args.warmup):
+        oracle.ring_allreduce_avg_f32(rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.ring_allreduce_avg_f32(rows)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = 2.0 * wl.n * p * 4 * args.steps / total / 1e9
+    sample = "ring of N=%d x P=%d fp32 elements (N(0,%g), seed %d) per step, in place" % (
+        wl.n, p, wl.scale, wl.seed)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "workers": wl.n, "elements_per_worker": p,
+                                        "note": "CPU oracle on a bounded sample of the workload"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    if args.gpus > 1 and ws == 1:
+        print("bench.py: --gpus %d needs torchrun (one process per GPU)" % args.gpus, file=sys.stderr)
+        return 2
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    from gradient_ring_all_gb300 import build
+    build.build()
+    import gradient_ring_all_gb300 as ra
+    import synth
+    ra.load()
+    wl = synth.WORKLOADS[WORKLOAD]
+    n, p = wl.n, wl.p
+    nbytes = wl.min_bytes  # 2 * N * P * 4
+
+    # inputs: each worker's row generated on the host, copied to its own allocation
+    rows = [torch.empty(p, dtype=torch.float32, device="cuda") for _ in range(n)]
+    piece = 1 << 26
+    host = torch.empty(piece, dtype=torch.float32).pin_memory()
+    for k in range(n):
+        for s in range(0, p, piece):
+            c = min(piece, p - s)
+            wl.fill_row(host.data_ptr(), k, s, c)
+            rows[k][s:s + c].copy_(host[:c])
+    del host
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ra.ra_allreduce_avg(rows, stream)
+    torch.cuda.synchronize()
+
+    # timed region: K launches, an event pair around each on the launch stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    clocks = _ClockSampler(local).start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_all0.record(stream)
+    for k in range(args.steps):
+        starts[k].record(stream)
+        ra.ra_allreduce_avg(rows, stream)
+        ends[k].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop(w0, w1)
+    total_ms = t_all0.elapsed_time(t_all1)
+    kern_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t[0])
+    ms_per_step = total_ms / args.steps
+    value = nbytes * ws / (ms_per_step / 1e3) / 1e9
+    avg_kernel_ms = sum(kern_ms) / len(kern_ms)
+
+    # end to end through the host-buffer entry point: pinned host rows ->
+    # device -> fused all-reduce -> every host row, every step
+    e2e_steps = max(1, min(args.steps, 10))
+    hrows = [torch.empty(p, dtype=torch.float32).pin_memory() for _ in range(n)]
+    for k in range(n):
+        hrows[k].copy_(rows[k])
+    ra.ra_allreduce_avg_host(hrows, rows, stream)  # warm-up
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        ra.ra_allreduce_avg_host(hrows, rows, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    del hrows
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = _peaks()
+    achieved = nbytes / (avg_kernel_ms / 1e3) / 1e9
+    cpu_gbs, cpu_s, reps = None, None, 16
+    if ws == 1:
+        cpu_gbs, cpu_s = _cpu_oracle_sample(n, CPU_SAMPLE_P, reps)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "workers": n, "elements_per_worker": p,
+                   "distribution": "N(0, %g), seed %d, worker n = generator stream n" % (wl.scale, wl.seed),
+                   "bytes_per_step": nbytes, "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "l2": "inputs of %.1f GB per GPU, larger than the 129 MB L2; no flush" % (n * p * 4 / 1e9)},
+        "pct_of_measured_hbm": 100.0 * value / ws / peak,
+        "pct_of_nominal_hbm": 100.0 * value / ws / NOMINAL_HBM_GBS,
+        "elements_per_s": n * p * ws / (ms_per_step / 1e3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "kernel": "fused_allreduce_kernel<F32, N=8>", "avg_launch_ms": avg_kernel_ms,
+                     "traffic": _traffic_from_profile("fused_f32_n8_speech300m")},
+        "e2e": {"value": nbytes * ws / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": n * p * 4, "d2h_bytes_per_step": n * p * 4,
+                "path": "ra_allreduce_avg_host: pinned host rows -> device -> fused kernel -> host rows"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if cpu_gbs is not None:
+        line["cpu_baseline"] = {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": "%d in-place runs of a ring of N=%d x P=%d fp32 elements (%.1f s)"
+                                          % (reps, n, CPU_SAMPLE_P, cpu_s),
+                                "host_cpus": os.cpu_count()}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,226 @@
+"""Python binding of the GB300 ring all-reduce library (C ABI in
+``include/ring_allreduce.h``).
+
+The functions carry the C names and only marshal arguments: every step of
+the all-reduce runs in the library's CUDA kernels.  PyTorch supplies device
+memory and streams.  Tensors must be contiguous CUDA tensors of one dtype
+(float32 or bfloat16) and one length; the current torch stream is used
+unless ``stream`` (a cudaStream_t as int, or a torch.cuda.Stream) is given.
+
+There is no CPU fallback: if the shared library is missing this module
+raises on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "RA_F32", "RA_BF16", "RA_MAX_N", "RaError", "library_path", "load",
+    "ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_staged_workspace_bytes",
+    "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
+]
+
+RA_F32 = 0
+RA_BF16 = 1
+RA_MAX_N = 64
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "lib", "libgradient_ring_all.so")
+_lib = None
+
+
+class RaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        lib = load()
+        name = lib.ra_status_str(status).decode()
+        msg = "%s failed: %s" % (what, name)
+        if name == "RA_ERR_CUDA":
+            msg += " (cudaError %d)" % lib.ra_last_cuda_error()
+        super().__init__(msg)
+        self.status = status
+
+
+class _Bucket(ctypes.Structure):
+    _fields_ = [("offset", ctypes.c_int64), ("count", ctypes.c_int64)]
+
+
+class _Traffic(ctypes.Structure):
+    _fields_ = [("sent", ctypes.c_int64), ("received", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libgradient_ring_all.so (build it with gradient_ring_all_gb300.build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError("libgradient_ring_all.so is not built (%s); run "
+                           "`python -m gradient_ring_all_gb300.build` first" % _LIB_PATH)
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    pvp = ctypes.POINTER(ctypes.c_void_p)
+    lib.ra_allreduce_avg.argtypes = [pvp, i32, i64, i32, vp]
+    lib.ra_allreduce_sgd.argtypes = [pvp, i32, i64, i32, vp, f32, vp]
+    lib.ra_staged_workspace_bytes.argtypes = [i32, i64, i32]
+    lib.ra_staged_workspace_bytes.restype = ctypes.c_size_t
+    lib.ra_allreduce_avg_staged.argtypes = [pvp, i32, i64, i32, vp, ctypes.c_size_t, ctypes.POINTER(_Traffic), vp]
+    lib.ra_bucket_plan.argtypes = [ctypes.POINTER(ctypes.c_int64), i32, i32, i64, ctypes.POINTER(_Bucket), i32,
+                                   ctypes.POINTER(i32)]
+    lib.ra_allreduce_avg_buckets.argtypes = [pvp, i32, i32, ctypes.POINTER(_Bucket), i32, vp]
+    lib.ra_allreduce_avg_host.argtypes = [pvp, pvp, i32, i64, i32, vp]
+    lib.ra_chunk_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.ra_chunk_range.restype = None
+    lib.ra_status_str.argtypes = [i32]
+    lib.ra_status_str.restype = ctypes.c_char_p
+    lib.ra_last_cuda_error.argtypes = []
+    for nm in ("ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_bucket_plan",
+               "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_last_cuda_error"):
+        getattr(lib, nm).restype = i32
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# marshalling
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return RA_F32
+    if t.dtype == torch.bfloat16:
+        return RA_BF16
+    raise TypeError("gradients must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _rows(tensors):
+    """(pointer array, n, p, dtype code) for a list of worker tensors, or raw
+    (pointers, p, dtype) when given ints."""
+    tensors = list(tensors)
+    if not tensors:
+        raise ValueError("need at least one worker buffer")
+    n = len(tensors)
+    t0 = tensors[0]
+    dt = _dtype_code(t0)
+    p = t0.numel()
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError("worker buffers must be CUDA tensors")
+        if t.dtype != t0.dtype or t.numel() != p or t.device != t0.device:
+            raise ValueError("worker buffers must share dtype, length and device")
+        if not t.is_contiguous():
+            raise ValueError("worker buffers must be contiguous")
+    arr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in tensors])
+    return arr, n, p, dt, t0.device
+
+
+def _stream(stream, device):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise RaError(status, what)
+
+
+# ---------------------------------------------------------------------------
+# the calls
+
+
+def ra_allreduce_avg(tensors, stream=None) -> None:
+    """Every worker tensor becomes the element-wise mean of all of them."""
+    arr, n, p, dt, dev = _rows(tensors)
+    _check(load().ra_allreduce_avg(arr, n, p, dt, _stream(stream, dev)), "ra_allreduce_avg")
+
+
+def ra_allreduce_sgd(tensors, w, lr: float, stream=None) -> None:
+    """ra_allreduce_avg plus w -= lr * mean in the same pass (w: float32 CUDA tensor)."""
+    import torch
+    arr, n, p, dt, dev = _rows(tensors)
+    if w.dtype != torch.float32 or w.numel() != p or not w.is_contiguous() or w.device != dev:
+        raise ValueError("w must be a contiguous float32 tensor of the gradients' length and device")
+    _check(load().ra_allreduce_sgd(arr, n, p, dt, ctypes.c_void_p(w.data_ptr()), float(lr), _stream(stream, dev)),
+           "ra_allreduce_sgd")
+
+
+def ra_staged_workspace_bytes(n: int, p: int, dtype: int) -> int:
+    return int(load().ra_staged_workspace_bytes(n, p, dtype))
+
+
+def ra_allreduce_avg_staged(tensors, workspace=None, stream=None):
+    """The literal 2(N-1)+1-launch ring; returns [(sent, received)] per worker.
+    `workspace` is a CUDA tensor of at least ra_staged_workspace_bytes bytes
+    (allocated here with torch when None and needed)."""
+    import torch
+    arr, n, p, dt, dev = _rows(tensors)
+    need = ra_staged_workspace_bytes(n, p, dt)
+    ws_ptr, ws_bytes = None, 0
+    if need > 0:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    traffic = (_Traffic * n)()
+    _check(load().ra_allreduce_avg_staged(arr, n, p, dt, ctypes.c_void_p(ws_ptr), ws_bytes, traffic,
+                                          _stream(stream, dev)), "ra_allreduce_avg_staged")
+    return [(traffic[k].sent, traffic[k].received) for k in range(n)]
+
+
+def ra_bucket_plan(numel, elem_bytes: int, cap_bytes: int):
+    """Reverse-order buckets of whole tensors, each >= cap_bytes but the last;
+    returns [(offset, count)] in elements of the forward-ordered flat array."""
+    numel = [int(x) for x in numel]
+    nt = len(numel)
+    arr = (ctypes.c_int64 * max(1, nt))(*numel)
+    out = (_Bucket * (nt + 1))()
+    nb = ctypes.c_int(0)
+    _check(load().ra_bucket_plan(arr, nt, elem_bytes, cap_bytes, out, nt + 1, ctypes.byref(nb)), "ra_bucket_plan")
+    return [(out[k].offset, out[k].count) for k in range(nb.value)]
+
+
+def ra_allreduce_avg_buckets(tensors, buckets, stream=None) -> None:
+    """Each (offset, count) bucket of the worker tensors is its own ring."""
+    arr, n, p, dt, dev = _rows(tensors)
+    for off, cnt in buckets:
+        if off < 0 or cnt < 0 or off + cnt > p:
+            raise ValueError("bucket (%d, %d) outside the %d-element buffers" % (off, cnt, p))
+    nb = len(buckets)
+    b = (_Bucket * max(1, nb))(*[_Bucket(int(o), int(c)) for o, c in buckets])
+    _check(load().ra_allreduce_avg_buckets(arr, n, dt, b, nb, _stream(stream, dev)), "ra_allreduce_avg_buckets")
+
+
+def ra_allreduce_avg_host(host_tensors, dev_tensors, stream=None) -> None:
+    """Host (ideally pinned) worker tensors -> device staging -> fused
+    all-reduce -> mean copied back to every host tensor, queued on the stream."""
+    arr, n, p, dt, dev = _rows(dev_tensors)
+    host_tensors = list(host_tensors)
+    if len(host_tensors) != n:
+        raise ValueError("need one host tensor per device staging tensor")
+    for h in host_tensors:
+        if h.is_cuda or h.numel() != p or h.dtype != dev_tensors[0].dtype or not h.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors matching the staging tensors")
+    harr = (ctypes.c_void_p * n)(*[h.data_ptr() for h in host_tensors])
+    _check(load().ra_allreduce_avg_host(harr, arr, n, p, dt, _stream(stream, dev)), "ra_allreduce_avg_host")
+
+
+def ra_chunk_range(p: int, n: int, c: int):
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    load().ra_chunk_range(p, n, c, ctypes.byref(b), ctypes.byref(e))
+    return b.value, e.value
+
+
+def ra_status_str(status: int) -> str:
+    return load().ra_status_str(status).decode()
+
+
+def ra_last_cuda_error() -> int:
+    return load().ra_last_cuda_error()

@@ -1,0 +1,61 @@
+// ra_fused_launch.cuh -- host-side launch of the fused kernel for one
+// element type (included by ra_fused_f32.cu and ra_fused_bf16.cu so the two
+// instantiation sets compile in parallel).
+#pragma once
+
+#include <string.h>
+
+#include "ra_kernels.cuh"
+
+namespace ra {
+
+template <class E, int NT, bool SGD, bool VEC, int MAXSEG>
+static cudaError_t fused_launch_one(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+    FusedParams<MAXSEG> p;
+    memset(&p, 0, sizeof(p));
+    for (int k = 0; k < L.n; ++k) p.rows[k] = L.rows[k];
+    p.w = L.w;
+    p.lr = L.lr;
+    p.n = L.n;
+    p.nseg = L.nseg;
+    p.mis = L.mis;
+    p.ntiles = ntiles;
+    for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
+    auto kern = fused_allreduce_kernel<E, NT, SGD, VEC, MAXSEG>;
+    int resident = 0;
+    cudaError_t err = resident_blocks(reinterpret_cast<const void *>(kern), &resident);
+    if (err != cudaSuccess) return err;
+    const int64_t grid = ntiles < resident ? ntiles : resident;
+    kern<<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <class E, int NT>
+static cudaError_t fused_launch_nt(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+    const bool sgd = L.w != nullptr;
+    const bool big = L.nseg > kSegSmall;
+    if (sgd && big) return cudaErrorInvalidValue;  // the SGD call has at most n segments
+    if (L.vector) {
+        if (sgd) return fused_launch_one<E, NT, true, true, kSegSmall>(L, ntiles, s);
+        if (big) return fused_launch_one<E, NT, false, true, kSegLarge>(L, ntiles, s);
+        return fused_launch_one<E, NT, false, true, kSegSmall>(L, ntiles, s);
+    }
+    // scalar path: generic worker count only
+    if (sgd) return fused_launch_one<E, 0, true, false, kSegSmall>(L, ntiles, s);
+    if (big) return fused_launch_one<E, 0, false, false, kSegLarge>(L, ntiles, s);
+    return fused_launch_one<E, 0, false, false, kSegSmall>(L, ntiles, s);
+}
+
+template <class E>
+static cudaError_t fused_launch_dtype(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+    switch (L.vector ? fused_compile_time_n(L.n) : 0) {
+        case 2: return fused_launch_nt<E, 2>(L, ntiles, s);
+        case 4: return fused_launch_nt<E, 4>(L, ntiles, s);
+        case 8: return fused_launch_nt<E, 8>(L, ntiles, s);
+        case 16: return fused_launch_nt<E, 16>(L, ntiles, s);
+        case 32: return fused_launch_nt<E, 32>(L, ntiles, s);
+        default: return fused_launch_nt<E, 0>(L, ntiles, s);
+    }
+}
+
+}  // namespace ra

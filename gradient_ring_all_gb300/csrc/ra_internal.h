@@ -1,0 +1,97 @@
+// ra_internal.h -- types shared by the library's host and device code.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ring_allreduce.h"
+
+namespace ra {
+
+// A contiguous element range in which every element belongs to ring chunk c
+// (so its scatter-reduce fold starts at worker c).  tile0 is the index of
+// the segment's first tile in the launch.
+struct Seg {
+    int64_t begin;
+    int64_t end;
+    int64_t tile0;
+    int32_t c;
+    int32_t pad;
+};
+static_assert(sizeof(Seg) == 32, "Seg layout");
+
+constexpr int kThreadsPerBlock = 256;
+constexpr int kScalarPerThread = 4;  // elements per thread per tile, scalar path
+constexpr int kStagedTileVec = 512;  // 16-byte vectors per tile, staged kernel
+
+// 16-byte vectors each thread keeps in flight per worker in the fused
+// kernel, by compile-time worker count (0 = any count)
+__host__ __device__ constexpr int fused_vec_per_thread(int nt) {
+    return nt == 0 ? 1 : (nt <= 4 ? 4 : (nt <= 8 ? 2 : 1));
+}
+
+__host__ __device__ constexpr int64_t fused_tile_vectors(int nt) {
+    return (int64_t)kThreadsPerBlock * fused_vec_per_thread(nt);
+}
+
+// The 16-byte-vector interior [ab, ae) of the element range [b, e) when the
+// rows' addresses are `mis` elements past a 16-byte boundary (V elements per
+// vector): ab is the first index >= b with (index + mis) % V == 0, ae the
+// last such index <= e; [b, ab) and [ae, e) are the scalar head and tail.
+__host__ __device__ inline void vector_interior(int64_t b, int64_t e, int mis, int V, int64_t *ab, int64_t *ae) {
+    int64_t r = (b + mis) % V;
+    int64_t up = r == 0 ? b : b + (V - r);
+    if (up > e) up = e;
+    int64_t down = e - (e + mis) % V;
+    if (down < up) down = up;
+    *ab = up;
+    *ae = down;
+}
+
+// kernel-parameter segment tables: a small one for plain calls and a large
+// one for bucketed calls (kernel parameters are limited to 32 KiB)
+constexpr int kSegSmall = RA_MAX_N;
+constexpr int kSegLarge = 896;
+
+enum StagedOp { kOpScatter = 0, kOpDivide = 1, kOpGather = 2 };
+
+struct FusedLaunch {
+    void *rows[RA_MAX_N];
+    int n;
+    int dtype;
+    float *w;  // null: plain average
+    float lr;
+    bool vector;
+    int mis;
+    const Seg *seg;  // host table, tile0 filled by the launcher
+    int nseg;
+};
+
+// fill seg[].tile0 and return the tile count for the fused kernel chosen
+// for (n, dtype, vector)
+int64_t fused_assign_tiles(Seg *seg, int nseg, int n, int dtype, bool vector, int mis);
+int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis);
+
+cudaError_t launch_fused_f32(const FusedLaunch &L, int64_t ntiles, cudaStream_t s);
+cudaError_t launch_fused_bf16(const FusedLaunch &L, int64_t ntiles, cudaStream_t s);
+
+// resident blocks per SM x SMs for a kernel on the current device (cached)
+cudaError_t resident_blocks(const void *kernel, int *out);
+
+struct StagedLaunch {
+    void *rows[RA_MAX_N];
+    float *msg;
+    int n;
+    int dtype;
+    bool vector;
+    int mis;
+    const Seg *seg;
+    int nseg;
+    int64_t ntiles;
+};
+cudaError_t launch_staged_step(const StagedLaunch &L, int op, int t, cudaStream_t s);
+
+int fused_compile_time_n(int n);  // the specialised worker count used for n (0 = generic)
+
+}  // namespace ra

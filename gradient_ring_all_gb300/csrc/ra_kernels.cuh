@@ -1,0 +1,455 @@
+// ra_kernels.cuh -- device code of the ring all-reduce library (sm_103a).
+//
+// Work decomposition.  The host cuts every request into "segments": a
+// contiguous element range of the workers' arrays in which every element
+// belongs to the same ring chunk c (Gibiansky, "Scatter-Reduce": the array
+// is split into N chunks, and the chunk decides where the scatter-reduce
+// starts accumulating it).  A plain all-reduce has N segments, a bucketed
+// one N per bucket.  Each segment is cut into tiles of kTileVec 16-byte
+// vectors; a persistent grid walks the tiles, finds the tile's segment by
+// binary search in the kernel-parameter table, and so knows c for the whole
+// tile.  The few elements of a segment that do not fill a 16-byte vector
+// (its ragged head and tail) are done with scalar accesses by the
+// segment's first and last tiles.
+//
+// Fused kernel (one pass): for each vector, load the N workers' values in
+// ring order starting at worker c, fold them left in binary32 (the order
+// in which the scatter-reduce adds them), divide by N, and store the mean
+// to all N workers (the all-gather's result).  Loads and stores use the
+// streaming cache hint: every byte is touched exactly once.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ra_internal.h"
+
+namespace ra {
+
+// ---------------------------------------------------------------------------
+// element types
+
+struct F32 {
+    using T = float;
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+};
+struct BF16 {
+    using T = uint16_t;  // bf16 bit pattern
+    static constexpr int kVec = 8;
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// binary32 -> bf16, round to nearest even (hardware conversion)
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+}
+
+// 16-byte vector load/store with the streaming (evict-first) hint.
+__device__ __forceinline__ uint4 ld_vec(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ void st_vec(void *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
+
+template <class E>
+__device__ __forceinline__ void unpack(uint4 v, float (&x)[E::kVec]);
+template <>
+__device__ __forceinline__ void unpack<F32>(uint4 v, float (&x)[4]) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+}
+template <>
+__device__ __forceinline__ void unpack<BF16>(uint4 v, float (&x)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        x[2 * k] = bf16_bits_to_f32(w[k] & 0xffffu);
+        x[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
+    }
+}
+
+// pack the binary32 mean into the stored vector; `back` receives the value
+// the workers will hold (for the SGD update)
+template <class E>
+__device__ __forceinline__ uint4 pack(const float (&x)[E::kVec], float (&back)[E::kVec]);
+template <>
+__device__ __forceinline__ uint4 pack<F32>(const float (&x)[4], float (&back)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) back[k] = x[k];
+    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+}
+template <>
+__device__ __forceinline__ uint4 pack<BF16>(const float (&x)[8], float (&back)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        w[k] = pack_bf16x2(x[2 * k], x[2 * k + 1]);
+        back[2 * k] = bf16_bits_to_f32(w[k] & 0xffffu);
+        back[2 * k + 1] = bf16_bits_to_f32(w[k] >> 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <class E>
+__device__ __forceinline__ float load_scalar(const void *row, int64_t i) {
+    if constexpr (sizeof(typename E::T) == 4)
+        return __ldcs(reinterpret_cast<const float *>(row) + i);
+    else
+        return bf16_bits_to_f32(__ldcs(reinterpret_cast<const unsigned short *>(row) + i));
+}
+
+// stores the mean, returns the value the workers hold
+template <class E>
+__device__ __forceinline__ float store_scalar_all(void *const *rows, int n, int64_t i, float avg) {
+    if constexpr (sizeof(typename E::T) == 4) {
+        for (int k = 0; k < n; ++k) __stcs(reinterpret_cast<float *>(rows[k]) + i, avg);
+        return avg;
+    } else {
+        const unsigned short b = (unsigned short)f32_to_bf16_bits(avg);
+        for (int k = 0; k < n; ++k) __stcs(reinterpret_cast<unsigned short *>(rows[k]) + i, b);
+        return bf16_bits_to_f32(b);
+    }
+}
+
+// Mean of a binary32 sum over n workers: one IEEE division, rounded to
+// nearest even.  For n a power of two, x * (1/n) is the same correctly
+// rounded value (1/n is exact, and both operations round the same real
+// number x/n), so the cheaper multiplication is used there.
+template <int NT>
+__device__ __forceinline__ float div_n(float x, int n) {
+    if constexpr (NT > 0 && (NT & (NT - 1)) == 0)
+        return __fmul_rn(x, 1.0f / (float)NT);
+    else
+        return __fdiv_rn(x, (float)(NT > 0 ? NT : n));
+}
+
+// worker index (c + k) mod n for 0 <= c, k < n
+__device__ __forceinline__ int ring_idx(int c, int k, int n) {
+    int r = c + k;
+    return r >= n ? r - n : r;
+}
+
+// ---------------------------------------------------------------------------
+// segment table
+
+template <int MAXSEG>
+struct FusedParams {
+    void *rows[RA_MAX_N];  // worker arrays (device)
+    float *w;              // SGD weights (device) or null
+    float lr;
+    int n;                 // workers
+    int nseg;
+    int mis;               // rows' common misalignment, in elements (< kVec); vector mode only
+    int64_t ntiles;
+    Seg seg[MAXSEG];
+};
+
+template <int MAXSEG>
+__device__ __forceinline__ int find_seg(const Seg *seg, int nseg, int64_t tile) {
+    // largest s with seg[s].tile0 <= tile
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (seg[mid].tile0 <= tile)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------
+// fused kernel
+
+// one element through the scalar path: ring-order fold from worker c
+template <class E, int NT, bool SGD, int MAXSEG>
+__device__ __forceinline__ void fused_scalar(const FusedParams<MAXSEG> &p, int c, int64_t i) {
+    const int n = NT > 0 ? NT : p.n;
+    float acc = load_scalar<E>(p.rows[c], i);
+    for (int k = 1; k < n; ++k) acc = __fadd_rn(load_scalar<E>(p.rows[ring_idx(c, k, n)], i), acc);
+    const float avg = div_n<NT>(acc, n);
+    const float held = store_scalar_all<E>(p.rows, n, i, avg);
+    if (SGD) p.w[i] = __fsub_rn(p.w[i], __fmul_rn(p.lr, held));
+}
+
+constexpr int kThreads = kThreadsPerBlock;
+
+template <class E, int NT, bool SGD, int MAXSEG>
+__device__ __forceinline__ void fused_vectors(const FusedParams<MAXSEG> &p, int c, int64_t i0, int64_t ae) {
+    constexpr int V = E::kVec;
+    constexpr int VPT = fused_vec_per_thread(NT);
+    const int n = NT > 0 ? NT : p.n;
+    constexpr int esz = (int)sizeof(typename E::T);
+
+    if constexpr (NT > 0) {
+        // all NT x VPT loads issued before any arithmetic
+        uint4 x[VPT][NT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t i = i0 + (int64_t)j * kThreads * V;
+            if (i < ae) {
+#pragma unroll
+                for (int k = 0; k < NT; ++k)
+                    x[j][k] = ld_vec(reinterpret_cast<const char *>(p.rows[ring_idx(c, k, NT)]) + i * esz);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int64_t i = i0 + (int64_t)j * kThreads * V;
+            if (i < ae) {
+                float acc[V], t[V];
+                unpack<E>(x[j][0], acc);
+#pragma unroll
+                for (int k = 1; k < NT; ++k) {
+                    unpack<E>(x[j][k], t);
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(t[e], acc[e]);
+                }
+                float avg[V], held[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) avg[e] = div_n<NT>(acc[e], n);
+                const uint4 out = pack<E>(avg, held);
+#pragma unroll
+                for (int k = 0; k < NT; ++k) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, out);
+                if constexpr (SGD) {
+#pragma unroll
+                    for (int e = 0; e < V; e += 4) {
+                        float4 *wp = reinterpret_cast<float4 *>(p.w + i + e);
+                        float4 wv = __ldcs(wp);
+                        wv.x = __fsub_rn(wv.x, __fmul_rn(p.lr, held[e + 0]));
+                        wv.y = __fsub_rn(wv.y, __fmul_rn(p.lr, held[e + 1]));
+                        wv.z = __fsub_rn(wv.z, __fmul_rn(p.lr, held[e + 2]));
+                        wv.w = __fsub_rn(wv.w, __fmul_rn(p.lr, held[e + 3]));
+                        __stcs(wp, wv);
+                    }
+                }
+            }
+        }
+    } else {
+        // any n: groups of 8 workers in flight at a time, same fold order
+        constexpr int G = 8;
+        const int64_t i = i0;
+        if (i >= ae) return;
+        float acc[V], t[V];
+        for (int k0 = 0; k0 < n; k0 += G) {
+            uint4 x[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                if (k0 + g < n)
+                    x[g] = ld_vec(reinterpret_cast<const char *>(p.rows[ring_idx(c, k0 + g, n)]) + i * esz);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                if (k0 + g < n) {
+                    if (k0 + g == 0) {
+                        unpack<E>(x[g], acc);
+                    } else {
+                        unpack<E>(x[g], t);
+#pragma unroll
+                        for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(t[e], acc[e]);
+                    }
+                }
+            }
+        }
+        float avg[V], held[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) avg[e] = div_n<0>(acc[e], n);
+        const uint4 out = pack<E>(avg, held);
+        for (int k = 0; k < n; ++k) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, out);
+        if constexpr (SGD) {
+#pragma unroll
+            for (int e = 0; e < V; e += 4) {
+                float4 *wp = reinterpret_cast<float4 *>(p.w + i + e);
+                float4 wv = __ldcs(wp);
+                wv.x = __fsub_rn(wv.x, __fmul_rn(p.lr, held[e + 0]));
+                wv.y = __fsub_rn(wv.y, __fmul_rn(p.lr, held[e + 1]));
+                wv.z = __fsub_rn(wv.z, __fmul_rn(p.lr, held[e + 2]));
+                wv.w = __fsub_rn(wv.w, __fmul_rn(p.lr, held[e + 3]));
+                __stcs(wp, wv);
+            }
+        }
+    }
+}
+
+// VECTOR: rows share their 16-byte misalignment (vector interior + scalar
+// edges); otherwise every element takes the scalar path.
+template <class E, int NT, bool SGD, bool VECTOR, int MAXSEG>
+__global__ void __launch_bounds__(kThreads) fused_allreduce_kernel(const __grid_constant__ FusedParams<MAXSEG> p) {
+    constexpr int V = E::kVec;
+    for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+        const int s = find_seg<MAXSEG>(p.seg, p.nseg, tile);
+        const Seg sg = p.seg[s];
+        const int c = sg.c;
+        const int64_t t_in_seg = tile - sg.tile0;
+        if constexpr (VECTOR) {
+            int64_t ab, ae;
+            vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
+            const int64_t i0 = ab + (t_in_seg * fused_tile_vectors(NT) + threadIdx.x) * V;
+            fused_vectors<E, NT, SGD>(p, c, i0, ae);
+            if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) fused_scalar<E, NT, SGD>(p, c, sg.begin + threadIdx.x);
+            const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
+            if (last && threadIdx.x < sg.end - ae) fused_scalar<E, NT, SGD>(p, c, ae + threadIdx.x);
+        } else {
+            const int64_t i0 = sg.begin + t_in_seg * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
+#pragma unroll 4
+            for (int j = 0; j < kScalarPerThread; ++j) {
+                const int64_t i = i0 + (int64_t)j * kThreads;
+                if (i < sg.end) fused_scalar<E, NT, SGD>(p, c, i);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// staged kernel: one ring iteration per launch
+
+struct StagedParams {
+    void *rows[RA_MAX_N];
+    float *msg;  // binary32 partial sums (bf16 only), element i at msg[i]
+    int n;
+    int t;       // iteration
+    int op;      // StagedOp
+    int mis;     // rows' (and msg's) common misalignment in elements (< kVec)
+    int nseg;
+    int64_t ntiles;
+    Seg seg[RA_MAX_N];
+};
+
+// One element of one staged iteration.  Chunk c's partial sits at worker
+// (c + t) mod n in scatter-reduce iteration t and moves to (c + t + 1) mod n;
+// the complete chunk sits at worker (c - 1) mod n; in all-gather iteration t
+// worker (c + t - 1) mod n sends it to worker (c + t) mod n.
+template <class E>
+__device__ __forceinline__ void staged_scalar(const StagedParams &p, int c, int64_t i) {
+    const int n = p.n;
+    switch (p.op) {
+        case kOpScatter: {  // receiver's own value + received partial
+            const int rcv = ring_idx(c, p.t + 1 >= n ? p.t + 1 - n : p.t + 1, n);
+            if constexpr (sizeof(typename E::T) == 4) {
+                const int snd = ring_idx(c, p.t, n);
+                float *d = reinterpret_cast<float *>(p.rows[rcv]);
+                d[i] = __fadd_rn(d[i], reinterpret_cast<const float *>(p.rows[snd])[i]);
+            } else {
+                const float own = load_scalar<E>(p.rows[rcv], i);
+                const float in = p.t == 0 ? load_scalar<E>(p.rows[c], i) : p.msg[i];
+                p.msg[i] = __fadd_rn(own, in);
+            }
+            break;
+        }
+        case kOpDivide: {
+            const int own = c == 0 ? n - 1 : c - 1;
+            if constexpr (sizeof(typename E::T) == 4) {
+                float *d = reinterpret_cast<float *>(p.rows[own]);
+                d[i] = __fdiv_rn(d[i], (float)n);
+            } else {
+                reinterpret_cast<unsigned short *>(p.rows[own])[i] =
+                    (unsigned short)f32_to_bf16_bits(__fdiv_rn(p.msg[i], (float)n));
+            }
+            break;
+        }
+        default: {  // kOpGather: overwrite
+            const int rcv = ring_idx(c, p.t, n);
+            const int snd = rcv == 0 ? n - 1 : rcv - 1;
+            using T = typename E::T;
+            reinterpret_cast<T *>(p.rows[rcv])[i] = reinterpret_cast<const T *>(p.rows[snd])[i];
+            break;
+        }
+    }
+}
+
+template <class E>
+__device__ __forceinline__ void staged_vector(const StagedParams &p, int c, int64_t i) {
+    const int n = p.n;
+    constexpr int V = E::kVec;
+    constexpr int esz = (int)sizeof(typename E::T);
+    switch (p.op) {
+        case kOpScatter: {
+            const int rcv = ring_idx(c, p.t + 1 >= n ? p.t + 1 - n : p.t + 1, n);
+            float own[V], in[V];
+            unpack<E>(ld_vec(reinterpret_cast<const char *>(p.rows[rcv]) + i * esz), own);
+            if constexpr (sizeof(typename E::T) == 4) {
+                const int snd = ring_idx(c, p.t, n);
+                unpack<E>(ld_vec(reinterpret_cast<const char *>(p.rows[snd]) + i * esz), in);
+                float s[V], back[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) s[e] = __fadd_rn(own[e], in[e]);
+                st_vec(reinterpret_cast<char *>(p.rows[rcv]) + i * esz, pack<E>(s, back));
+            } else {
+                if (p.t == 0) {
+                    unpack<E>(ld_vec(reinterpret_cast<const char *>(p.rows[c]) + i * esz), in);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < V; e += 4) {
+                        const float4 m = __ldcs(reinterpret_cast<const float4 *>(p.msg + i + e));
+                        in[e] = m.x, in[e + 1] = m.y, in[e + 2] = m.z, in[e + 3] = m.w;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < V; e += 4)
+                    __stcs(reinterpret_cast<float4 *>(p.msg + i + e),
+                           make_float4(__fadd_rn(own[e], in[e]), __fadd_rn(own[e + 1], in[e + 1]),
+                                       __fadd_rn(own[e + 2], in[e + 2]), __fadd_rn(own[e + 3], in[e + 3])));
+            }
+            break;
+        }
+        case kOpDivide: {
+            const int own = c == 0 ? n - 1 : c - 1;
+            float s[V], q[V], back[V];
+            if constexpr (sizeof(typename E::T) == 4) {
+                unpack<E>(ld_vec(reinterpret_cast<const char *>(p.rows[own]) + i * esz), s);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; e += 4) {
+                    const float4 m = __ldcs(reinterpret_cast<const float4 *>(p.msg + i + e));
+                    s[e] = m.x, s[e + 1] = m.y, s[e + 2] = m.z, s[e + 3] = m.w;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < V; ++e) q[e] = __fdiv_rn(s[e], (float)n);
+            st_vec(reinterpret_cast<char *>(p.rows[own]) + i * esz, pack<E>(q, back));
+            break;
+        }
+        default: {
+            const int rcv = ring_idx(c, p.t, n);
+            const int snd = rcv == 0 ? n - 1 : rcv - 1;
+            st_vec(reinterpret_cast<char *>(p.rows[rcv]) + i * esz,
+                   ld_vec(reinterpret_cast<const char *>(p.rows[snd]) + i * esz));
+            break;
+        }
+    }
+}
+
+template <class E, bool VECTOR>
+__global__ void __launch_bounds__(kThreads) staged_step_kernel(const __grid_constant__ StagedParams p) {
+    constexpr int V = E::kVec;
+    for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+        const int s = find_seg<RA_MAX_N>(p.seg, p.nseg, tile);
+        const Seg sg = p.seg[s];
+        const int64_t t_in_seg = tile - sg.tile0;
+        if constexpr (VECTOR) {
+            int64_t ab, ae;
+            vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
+            const int64_t i0 = ab + (t_in_seg * kStagedTileVec + threadIdx.x) * V;
+#pragma unroll
+            for (int j = 0; j < kStagedTileVec / kThreads; ++j) {
+                const int64_t i = i0 + (int64_t)j * kThreads * V;
+                if (i < ae) staged_vector<E>(p, sg.c, i);
+            }
+            if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) staged_scalar<E>(p, sg.c, sg.begin + threadIdx.x);
+            const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
+            if (last && threadIdx.x < sg.end - ae) staged_scalar<E>(p, sg.c, ae + threadIdx.x);
+        } else {
+            const int64_t i0 = sg.begin + t_in_seg * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
+            for (int j = 0; j < kScalarPerThread; ++j) {
+                const int64_t i = i0 + (int64_t)j * kThreads;
+                if (i < sg.end) staged_scalar<E>(p, sg.c, i);
+            }
+        }
+    }
+}
+
+}  // namespace ra

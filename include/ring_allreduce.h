@@ -1,0 +1,194 @@
+/*
+ * ring_allreduce.h -- C ABI of the GB300 ring all-reduce library
+ * (libgradient_ring_all.so).
+ *
+ * The library computes the data-parallel gradient all-reduce-average of the
+ * ring algorithm for N logical workers whose gradient arrays all sit in the
+ * HBM of one GPU.  The result is what the ring of
+ *   Gibiansky, "Bringing HPC Techniques to Deep Learning" (Korean
+ *   translation), sections "Ring Allreduce", "Scatter-Reduce", "Allgather"
+ * leaves on every worker, divided by N so that every worker holds the mean
+ * gradient ("The Communication Problem": the GPUs average their gradients;
+ * "[PyTorch] GPU 분산 학습 1 - DP / DDP / FSDP 개념", section DDP: every GPU
+ * ends with the identical gradient).
+ *
+ * Numerics (identical bits to a step-by-step simulation of the ring):
+ *   - the array of P elements is split into N chunks; chunk c is
+ *     [c*q + min(c,r), (c+1)*q + min(c+1,r)), q = P / N, r = P mod N;
+ *   - element i of chunk c is summed in binary32 in ring order, a left fold
+ *     that starts at worker c: ((g_c + g_{c+1}) + g_{c+2}) + ... + g_{c+N-1}
+ *     (worker indices mod N) -- the order in which the scatter-reduce
+ *     accumulates it;
+ *   - the sum is divided by N with one IEEE binary32 division (round to
+ *     nearest even);
+ *   - bf16 gradients are widened exactly, summed in binary32 and the mean is
+ *     rounded to bf16 (nearest even) once;
+ *   - the SGD variant computes w - (lr * avg) with two roundings.
+ *
+ * Conventions shared by every call:
+ *   - `bufs` is a HOST array of n DEVICE pointers, one per worker; each
+ *     points at p elements of `dtype`, element-aligned.  The array itself
+ *     is read during the call only.  The buffers must not overlap.
+ *   - All device memory is owned by the caller and must stay valid until
+ *     the work queued on `stream` has finished.  Calls are asynchronous on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - Arguments are checked before anything is queued; a non-OK status
+ *     means nothing was launched.  RA_ERR_CUDA reports a failed launch or
+ *     device query; ra_last_cuda_error() returns its cudaError_t value.
+ *   - n == 1 or p == 0: nothing to reduce, RA_OK without a launch (x / 1 is
+ *     exact).  The SGD call still updates w when n == 1.
+ *   - Pointers whose addresses agree modulo 16 bytes take the 128-bit
+ *     vector path; any other element-aligned pointers take a scalar path
+ *     with the same results.
+ *   - Every function is thread-safe; the library keeps no state besides
+ *     a per-device cache of launch sizes.
+ */
+#ifndef RING_ALLREDUCE_H
+#define RING_ALLREDUCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
+
+typedef enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = 1, /* null pointer, n out of range, p < 0, bad dtype, misaligned element */
+    RA_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
+    RA_ERR_OVERLAP = 3,     /* two buffers (or w and a buffer) share bytes */
+    RA_ERR_CUDA = 4,        /* a CUDA call failed; see ra_last_cuda_error() */
+    RA_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait gave up */
+} ra_status;
+
+/* A contiguous element range [offset, offset + count) of every worker's array. */
+typedef struct {
+    int64_t offset;
+    int64_t count;
+} ra_bucket;
+
+/* Elements one worker sent and received over a full ring all-reduce. */
+typedef struct {
+    int64_t sent;
+    int64_t received;
+} ra_traffic;
+
+#define RA_MAX_N 64 /* most workers one call accepts */
+
+/*
+ * ra_allreduce_avg -- every worker's array becomes the element-wise mean of
+ * all n arrays (scatter-reduce, divide by N, all-gather; Gibiansky,
+ * "Scatter-Reduce" and "Allgather").  One fused pass: each element's n
+ * values are read once and the mean is written to all n arrays.
+ *   bufs   host array of n device pointers, p elements each, in place
+ *   n      1 .. RA_MAX_N workers
+ *   p      elements per worker (>= 0)
+ *   dtype  RA_F32 or RA_BF16
+ *   stream cudaStream_t to queue the kernel on
+ */
+ra_status ra_allreduce_avg(void *const *bufs, int n, int64_t p, int dtype, void *stream);
+
+/*
+ * ra_allreduce_sgd -- ra_allreduce_avg plus the synchronous SGD step
+ * w <- w - lr * avg in the same pass (Gibiansky, "The Communication
+ * Problem": the averaged gradient is applied to the weights; DDP: every
+ * replica applies the same update, so one binary32 weight copy stands for
+ * all of them).
+ *   w      device pointer to p binary32 weights, updated in place; must
+ *          not overlap any gradient buffer
+ *   lr     learning rate
+ * With RA_BF16 gradients the update uses the bf16-rounded mean.
+ */
+ra_status ra_allreduce_sgd(void *const *bufs, int n, int64_t p, int dtype, float *w, float lr, void *stream);
+
+/*
+ * ra_staged_workspace_bytes -- device workspace ra_allreduce_avg_staged
+ * needs: 0 for RA_F32 (the partial sums live in the workers' own arrays),
+ * p * 4 + 64 bytes for RA_BF16 (the binary32 partial sums "on the wire").
+ */
+size_t ra_staged_workspace_bytes(int n, int64_t p, int dtype);
+
+/*
+ * ra_allreduce_avg_staged -- the same result as ra_allreduce_avg, computed
+ * the way the ring moves data: N-1 scatter-reduce iterations (in iteration
+ * t every worker m adds the chunk (m-1-t) mod N it receives from worker
+ * m-1), one division step by the worker holding each complete chunk, and
+ * N-1 all-gather iterations (worker m overwrites chunk (m-t) mod N with its
+ * left neighbour's copy); one kernel launch per iteration, 2(N-1)+1 in all
+ * (Gibiansky, "Scatter-Reduce" and "Allgather", first-iteration tables).
+ *   ws, ws_bytes  device workspace of at least
+ *                 ra_staged_workspace_bytes(n, p, dtype) bytes (may be
+ *                 NULL when that is 0); owned by the caller
+ *   per_worker    optional HOST array of n ra_traffic entries; receives the
+ *                 elements each worker sent and received (Gibiansky,
+ *                 "Allreduce Communication Cost": 2(N-1)/N * P each when N
+ *                 divides P)
+ */
+ra_status ra_allreduce_avg_staged(void *const *bufs, int n, int64_t p, int dtype, void *ws, size_t ws_bytes,
+                                  ra_traffic *per_worker, void *stream);
+
+/*
+ * ra_bucket_plan -- groups layer tensors into buckets for per-subset
+ * all-reduce, output layer first (Gibiansky, "Applying the Allreduce to
+ * Deep Learning": the all-reduce can start on the output layer's
+ * parameters while backpropagation is still computing earlier layers).
+ * Rule: walk the tensors from the last to the first, add each to the open
+ * bucket and close the bucket once it holds >= cap_bytes; what is left
+ * forms the last bucket.  Buckets are contiguous element ranges of the
+ * forward-ordered flat array, written to out[] in closing order.
+ *   numel      host array of ntensors element counts (forward order)
+ *   elem_bytes bytes per element (> 0); cap_bytes > 0
+ *   out        host array of max_out entries; *n_out receives the count
+ * RA_ERR_INVALID_ARG if max_out is too small or an argument is bad.
+ */
+ra_status ra_bucket_plan(const int64_t *numel, int ntensors, int elem_bytes, int64_t cap_bytes, ra_bucket *out,
+                         int max_out, int *n_out);
+
+/*
+ * ra_allreduce_avg_buckets -- every bucket of every worker's array is
+ * all-reduced-averaged as a ring of its own (its own P = count and its own
+ * N chunks).  The (bucket, chunk) pieces go to the fused kernel in as few
+ * launches as the kernel-parameter space allows (at most 896 pieces per
+ * launch); the result does not depend on that split.
+ *   bufs   host array of n device pointers; each buffer must hold every
+ *          bucket, i.e. at least max(offset + count) elements
+ *   b, nb  host array of nb buckets (offset >= 0, count >= 0); buckets
+ *          must not overlap one another (RA_ERR_OVERLAP)
+ */
+ra_status ra_allreduce_avg_buckets(void *const *bufs, int n, int dtype, const ra_bucket *b, int nb, void *stream);
+
+/*
+ * ra_allreduce_avg_host -- ra_allreduce_avg for workers whose gradients
+ * live in HOST memory: copies every host array to its device staging
+ * buffer, runs the fused all-reduce there, and copies the mean back to
+ * every host array, all queued on `stream` (the end-to-end path of a
+ * data-parallel step whose gradients start and end on the host).
+ *   host_bufs  host array of n HOST pointers, p elements each; page-locked
+ *              memory makes the copies asynchronous, pageable memory works
+ *              but the CUDA runtime then copies synchronously
+ *   dev_bufs   host array of n DEVICE pointers, p elements each (caller-owned
+ *              staging; they end holding the mean as well)
+ * The host arrays must not be read before the stream has finished.
+ */
+ra_status ra_allreduce_avg_host(void *const *host_bufs, void *const *dev_bufs, int n, int64_t p, int dtype,
+                                void *stream);
+
+/* ra_chunk_range -- [begin, end) of chunk c of a p-element array split for
+ * n workers (the first p mod n chunks hold one extra element). */
+void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end);
+
+/* ra_status_str -- a static, human-readable name for a status. */
+const char *ra_status_str(int status);
+
+/* ra_last_cuda_error -- the cudaError_t behind this thread's most recent
+ * RA_ERR_CUDA (0 if none). */
+int ra_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RING_ALLREDUCE_H */

@@ -64,6 +64,8 @@ def _load():
     lib.oracle_sgd_update_bf16avg.restype = None
     lib.oracle_ring_avg_point_f32.argtypes = [vp, i32, i64, i64]
     lib.oracle_ring_avg_point_f32.restype = ctypes.c_float
+    lib.oracle_ring_avg_point_bf16.argtypes = [vp, i32, i64, i64]
+    lib.oracle_ring_avg_point_bf16.restype = ctypes.c_uint16
     lib.oracle_mean_f64.argtypes = [vp, i32, i64, vp]
     lib.oracle_mean_f64.restype = None
     lib.oracle_bucket_plan.argtypes = [vp, i32, i64, i64, vp, vp, i32]
@@ -179,6 +181,12 @@ def ring_avg_point_f32(vals, p: int, i: int) -> np.float32:
     """Ring result at element i of a p-element ring, from the N inputs at i."""
     v = np.ascontiguousarray(vals, dtype=np.float32)
     return np.float32(_load().oracle_ring_avg_point_f32(_ptr(v), v.shape[0], p, i))
+
+
+def ring_avg_point_bf16(vals, p: int, i: int) -> int:
+    """bf16 ring result (bit pattern) at element i, from the N bf16 inputs at i."""
+    v = np.ascontiguousarray(vals, dtype=np.uint16)
+    return int(_load().oracle_ring_avg_point_bf16(_ptr(v), v.shape[0], p, i))
 
 
 def mean_f64(rows):

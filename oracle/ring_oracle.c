@@ -340,3 +340,14 @@ void oracle_ring_traffic(int n_workers, int64_t p, int64_t *sent, int64_t *recei
                 received[mod_n((int64_t)n + 1, N)] += e - b;
             }
 }
+
+/* bf16 point evaluation: inputs are bf16 bit patterns, widened exactly; the
+ * binary32 ring result is rounded to bf16 once (the bf16 reading above). */
+uint16_t oracle_ring_avg_point_bf16(const uint16_t *vals, int n_workers, int64_t p, int64_t i) {
+    float wide[1024];
+    if (n_workers < 1 || n_workers > 1024)
+        return 0;
+    for (int n = 0; n < n_workers; ++n)
+        wide[n] = bf16_to_f32(vals[n]);
+    return oracle_f32_to_bf16(oracle_ring_avg_point_f32(wide, n_workers, p, i));
+}

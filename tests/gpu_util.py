@@ -1,0 +1,81 @@
+"""Helpers for the GPU parity tests: put seeded host rows on the device in
+the layouts the tests need, and read sampled outputs back."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+
+
+def to_device_rows(host_rows, layout="separate", pad=0):
+    """Copy host rows (float32 or uint16 bf16 bits) to CUDA tensors.
+
+    layout "separate": one allocation per worker (16-byte aligned);
+    "offset": one allocation per worker, each starting `pad` elements past a
+    16-byte boundary (all rows share the misalignment);
+    "mixed": row k starts (k * pad) mod 8 elements past a boundary, so the
+    rows disagree and the scalar path runs;
+    "packed": all rows back to back in one [N, P] allocation (rows start at
+    k*P elements, aligned only if P is a multiple of the vector).
+    """
+    n = len(host_rows)
+    p = host_rows[0].shape[0]
+    bf16 = host_rows[0].dtype == np.uint16
+    tdt = torch.bfloat16 if bf16 else torch.float32
+
+    def dev(a):
+        t = torch.from_numpy(a.view(np.int16) if bf16 else a)
+        return t.view(torch.bfloat16) if bf16 else t
+
+    if layout == "packed":
+        big = torch.empty(n * p + 8, dtype=tdt, device="cuda")
+        rows = [big[k * p:(k + 1) * p] for k in range(n)]
+    else:
+        rows = []
+        for k in range(n):
+            off = pad if layout == "offset" else ((k * pad) % 8 if layout == "mixed" else 0)
+            base = torch.empty(p + 16, dtype=tdt, device="cuda")
+            rows.append(base[off:off + p])
+    for k in range(n):
+        rows[k].copy_(dev(host_rows[k]))
+    return rows
+
+
+def to_host(t):
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def sample_indices(p, n, rng, count=2000, extra=()):
+    """Random indices plus every chunk boundary neighbourhood and the ends."""
+    idx = set(rng.integers(0, p, count).tolist()) if p > 0 else set()
+    from oracle import chunk_range  # host-side index arithmetic of the oracle
+    for c in range(n):
+        b, e = chunk_range(p, n, c)
+        for i in range(b - 9, b + 9):
+            if 0 <= i < p:
+                idx.add(i)
+    for i in list(range(16)) + list(range(p - 16, p)) + list(extra):
+        if 0 <= i < p:
+            idx.add(i)
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+def fill_device_rows(wl, rows, chunk_elems=1 << 26):
+    """Generate workload rows on the host in pieces and copy them to `rows`."""
+    p = wl.p
+    bf16 = wl.dtype == "bf16"
+    host = torch.empty(min(p, chunk_elems), dtype=torch.int16 if bf16 else torch.float32).pin_memory()
+    for k, r in enumerate(rows):
+        for s in range(0, p, chunk_elems):
+            cnt = min(chunk_elems, p - s)
+            wl.fill_row(host.data_ptr(), k, s, cnt)
+            src = host[:cnt].view(torch.bfloat16) if bf16 else host[:cnt]
+            r[s:s + cnt].copy_(src, non_blocking=False)
+
+
+def gather(rows, idx):
+    it = torch.from_numpy(idx).to("cuda")
+    return [to_host(r.index_select(0, it)) for r in rows]

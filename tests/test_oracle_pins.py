@@ -439,6 +439,16 @@ def test_bf16_ring_rounds_the_exact_mean_once(n):
             assert X.bf16_value(r[i]) == want
 
 
+def test_bf16_point_evaluation_matches_the_full_ring():
+    import synth
+    for n, p in [(2, 9), (5, 101), (16, 333)]:
+        rows = [synth.student_t3_bf16(3, w, 1e-3, 0, p) for w in range(n)]
+        g = [r.copy() for r in rows]
+        oracle.ring_allreduce_avg_bf16(rows)
+        for i in range(p):
+            assert oracle.ring_avg_point_bf16(np.array([r[i] for r in g], np.uint16), p, i) == rows[0][i]
+
+
 def test_bf16_partials_stay_binary32():
     # With bf16 partials the sum 256 + 1 + 1 would lose the ones (bf16 keeps
     # 8 significand bits); with binary32 partials the mean is (258)/3 = 86.
