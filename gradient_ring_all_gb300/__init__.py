@@ -18,12 +18,14 @@ import os
 __all__ = [
     "RA_F32", "RA_BF16", "RA_MAX_N", "RaError", "library_path", "load",
     "ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_staged_workspace_bytes",
-    "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
+    "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
+    "RA_STAGED_STATIC_MAX_P", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
 ]
 
 RA_F32 = 0
 RA_BF16 = 1
 RA_MAX_N = 64
+RA_STAGED_STATIC_MAX_P = 4194304
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libgradient_ring_all.so")
@@ -73,13 +75,15 @@ def load():
                                    ctypes.POINTER(i32)]
     lib.ra_allreduce_avg_buckets.argtypes = [pvp, i32, i32, ctypes.POINTER(_Bucket), i32, vp]
     lib.ra_allreduce_avg_host.argtypes = [pvp, pvp, i32, i64, i32, vp]
+    lib.ra_allreduce_avg_staged_static.argtypes = [pvp, i32, i64, i32, ctypes.POINTER(_Traffic), vp]
     lib.ra_chunk_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.ra_chunk_range.restype = None
     lib.ra_status_str.argtypes = [i32]
     lib.ra_status_str.restype = ctypes.c_char_p
     lib.ra_last_cuda_error.argtypes = []
     for nm in ("ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_bucket_plan",
-               "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_last_cuda_error"):
+               "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
+               "ra_last_cuda_error"):
         getattr(lib, nm).restype = i32
     _lib = lib
     return lib
@@ -172,6 +176,18 @@ def ra_allreduce_avg_staged(tensors, workspace=None, stream=None):
     traffic = (_Traffic * n)()
     _check(load().ra_allreduce_avg_staged(arr, n, p, dt, ctypes.c_void_p(ws_ptr), ws_bytes, traffic,
                                           _stream(stream, dev)), "ra_allreduce_avg_staged")
+    return [(traffic[k].sent, traffic[k].received) for k in range(n)]
+
+
+def ra_allreduce_avg_staged_static(tensors, stream=None):
+    """The staged ring without a workspace argument, for callers that cannot
+    allocate device memory: the bf16 partial sums use a scratch array built
+    into the library (at most RA_STAGED_STATIC_MAX_P elements per worker for
+    bf16).  Returns [(sent, received)] per worker."""
+    arr, n, p, dt, dev = _rows(tensors)
+    traffic = (_Traffic * n)()
+    _check(load().ra_allreduce_avg_staged_static(arr, n, p, dt, traffic, _stream(stream, dev)),
+           "ra_allreduce_avg_staged_static")
     return [(traffic[k].sent, traffic[k].received) for k in range(n)]
 
 

@@ -95,6 +95,8 @@ ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, con
 
 }  // namespace
 
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
 int fused_compile_time_n(int n) {
     switch (n) {
         case 2: case 4: case 8: case 16: case 32: return n;

@@ -94,4 +94,7 @@ cudaError_t launch_staged_step(const StagedLaunch &L, int op, int t, cudaStream_
 
 int fused_compile_time_n(int n);  // the specialised worker count used for n (0 = generic)
 
+// set the value ra_last_cuda_error() reports on this thread
+void record_cuda_error(cudaError_t e);
+
 }  // namespace ra

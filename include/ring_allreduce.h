@@ -161,6 +161,37 @@ ra_status ra_bucket_plan(const int64_t *numel, int ntensors, int elem_bytes, int
 ra_status ra_allreduce_avg_buckets(void *const *bufs, int n, int dtype, const ra_bucket *b, int nb, void *stream);
 
 /*
+ * ra_allreduce_avg_staged_static -- the same staged ring as
+ * ra_allreduce_avg_staged, for callers that cannot allocate device memory:
+ * the call takes no workspace and allocates nothing (no cudaMalloc/cudaFree,
+ * no allocating library routine).  The pages have no counterpart; this is
+ * an interface convenience of this library.
+ *
+ * Who needs it: code that runs inside a host framework which owns all device
+ * memory through its own pool and does not let plug-ins call cudaMalloc;
+ * latency-critical loops where cudaMalloc/cudaFree would synchronise the
+ * device; and programs whose device-memory budget is fixed when they start.
+ *
+ * How: the bf16 ring's binary32 partial sums go to a scratch array compiled
+ * into the library (RA_STAGED_STATIC_MAX_P binary32 elements, 16 MiB), which
+ * every GPU that loads the library holds until the process exits.  RA_F32
+ * needs no scratch (its partial sums live in the workers' own arrays).
+ *   bufs, n, p, dtype, per_worker, stream  as for ra_allreduce_avg_staged
+ * Returns RA_ERR_UNSUPPORTED, before doing anything, when dtype is RA_BF16
+ * and p > RA_STAGED_STATIC_MAX_P.
+ * The first call on a device (that passes the argument checks) looks up the
+ * array's device address and the launch size and caches them; make that
+ * first call before any stream capture.  All calls on a device share the
+ * array and it keeps the last call's contents; nothing in it needs clearing
+ * (each call writes every partial sum before reading it), but calls whose
+ * work overlaps on the GPU race on it: order them on one stream or with
+ * events.
+ */
+#define RA_STAGED_STATIC_MAX_P 4194304
+ra_status ra_allreduce_avg_staged_static(void *const *bufs, int n, int64_t p, int dtype, ra_traffic *per_worker,
+                                         void *stream);
+
+/*
  * ra_allreduce_avg_host -- ra_allreduce_avg for workers whose gradients
  * live in HOST memory: copies every host array to its device staging
  * buffer, runs the fused all-reduce there, and copies the mean back to
