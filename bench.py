@@ -195,8 +195,8 @@ def run_ours(args):
     import synth
     ra.load()
     wl = synth.WORKLOADS[WORKLOAD]
-    n, p = wl.n, wl.p
-    nbytes = wl.min_bytes  # 2 * N * P * 4
+    n, p = wl.n, (args.elements or wl.p)
+    nbytes = 2 * n * p * 4  # every input read once, the mean written to every worker once
 
     # inputs: each worker's row generated on the host, copied to its own allocation
     rows = [torch.empty(p, dtype=torch.float32, device="cuda") for _ in range(n)]
@@ -247,28 +247,46 @@ def run_ours(args):
     value = nbytes * ws / (ms_per_step / 1e3) / 1e9
     avg_kernel_ms = sum(kern_ms) / len(kern_ms)
 
-    # end to end through the host-buffer entry point: pinned host rows ->
-    # device -> fused all-reduce -> every host row, every step
+    if args.legs == "device":
+        # profiling runs (e.g. a smaller --elements under ncu): device loop only
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "workload": WORKLOAD, "workers": n, "elements_per_worker": p,
+                              "ms_per_step": total_ms / args.steps,
+                              "gbs": nbytes / (total_ms / args.steps / 1e3) / 1e9}), flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    # end to end through the host-buffer entry point: every step the fused
+    # kernel reads the 8 pinned host rows and writes the mean back to all of
+    # them over NVLink-C2C (the direct path); the staged path (copy in,
+    # reduce, copy out on the copy engines) is timed beside it for context
     e2e_steps = max(1, min(args.steps, 10))
     hrows = [torch.empty(p, dtype=torch.float32).pin_memory() for _ in range(n)]
     for k in range(n):
         hrows[k].copy_(rows[k])
-    ra.ra_allreduce_avg_host(hrows, rows, stream)  # warm-up
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        ra.ra_allreduce_avg_host(hrows, rows, stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+
+    def time_host(mode, steps):
+        ra.ra_allreduce_avg_host(hrows, rows, mode, stream)  # warm-up
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(steps):
+            ra.ra_allreduce_avg_host(hrows, rows, mode, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        if dist:
+            t = torch.tensor([ms], dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t[0])
+        return ms
+
+    e2e_ms = time_host(ra.RA_HOST_DIRECT, e2e_steps)
+    staged_ms = time_host(ra.RA_HOST_STAGED, max(1, e2e_steps // 2))
     del hrows
 
     if rank != 0:
@@ -298,10 +316,15 @@ def run_ours(args):
                      "traffic": _traffic_from_profile("fused_f32_n8_speech300m")},
         "e2e": {"value": nbytes * ws / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": n * p * 4, "d2h_bytes_per_step": n * p * 4,
-                "path": "ra_allreduce_avg_host: pinned host rows -> device -> fused kernel -> host rows"},
+                "path": "ra_allreduce_avg_host, direct: the fused kernel reads the pinned host rows and "
+                        "writes the mean back to every host row over NVLink-C2C"},
+        "e2e_staged": {"value": nbytes * ws / (staged_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": staged_ms,
+                       "path": "ra_allreduce_avg_host, staged: cudaMemcpyAsync in, fused kernel, cudaMemcpyAsync out"},
         "gpu_launches": args.steps,
         "clocks": clk,
     }
+    if args.elements:
+        line["config"]["note"] = "reduced --elements: not the benchmark configuration"
     if cpu_gbs is not None:
         line["cpu_baseline"] = {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": "%d in-place runs of a ring of N=%d x P=%d fp32 elements (%.1f s)"
@@ -319,6 +342,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--elements", type=int, default=0,
+                    help="profiling only: elements per worker instead of the workload's 300M")
+    ap.add_argument("--legs", choices=["all", "device"], default="all",
+                    help="profiling only: 'device' skips the end-to-end and CPU legs")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -19,13 +19,14 @@ __all__ = [
     "RA_F32", "RA_BF16", "RA_MAX_N", "RaError", "library_path", "load",
     "ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_staged_workspace_bytes",
     "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
-    "RA_STAGED_STATIC_MAX_P", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
+    "RA_STAGED_STATIC_MAX_P", "RA_HOST_AUTO", "RA_HOST_DIRECT", "RA_HOST_STAGED", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
 ]
 
 RA_F32 = 0
 RA_BF16 = 1
 RA_MAX_N = 64
 RA_STAGED_STATIC_MAX_P = 4194304
+RA_HOST_AUTO, RA_HOST_DIRECT, RA_HOST_STAGED = 0, 1, 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libgradient_ring_all.so")
@@ -74,7 +75,7 @@ def load():
     lib.ra_bucket_plan.argtypes = [ctypes.POINTER(ctypes.c_int64), i32, i32, i64, ctypes.POINTER(_Bucket), i32,
                                    ctypes.POINTER(i32)]
     lib.ra_allreduce_avg_buckets.argtypes = [pvp, i32, i32, ctypes.POINTER(_Bucket), i32, vp]
-    lib.ra_allreduce_avg_host.argtypes = [pvp, pvp, i32, i64, i32, vp]
+    lib.ra_allreduce_avg_host.argtypes = [pvp, pvp, i32, i64, i32, i32, vp]
     lib.ra_allreduce_avg_staged_static.argtypes = [pvp, i32, i64, i32, ctypes.POINTER(_Traffic), vp]
     lib.ra_chunk_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.ra_chunk_range.restype = None
@@ -214,18 +215,32 @@ def ra_allreduce_avg_buckets(tensors, buckets, stream=None) -> None:
     _check(load().ra_allreduce_avg_buckets(arr, n, dt, b, nb, _stream(stream, dev)), "ra_allreduce_avg_buckets")
 
 
-def ra_allreduce_avg_host(host_tensors, dev_tensors, stream=None) -> None:
-    """Host (ideally pinned) worker tensors -> device staging -> fused
-    all-reduce -> mean copied back to every host tensor, queued on the stream."""
-    arr, n, p, dt, dev = _rows(dev_tensors)
+def ra_allreduce_avg_host(host_tensors, dev_tensors=None, mode=RA_HOST_AUTO, stream=None) -> None:
+    """Every host (CPU) worker tensor becomes the mean.  The fused kernel works
+    on the host memory directly when the device can address it (pinned
+    memory, or any memory on a device that walks the host page tables);
+    otherwise -- or with mode=RA_HOST_STAGED -- through the device staging
+    tensors."""
+    import torch
     host_tensors = list(host_tensors)
-    if len(host_tensors) != n:
-        raise ValueError("need one host tensor per device staging tensor")
+    if not host_tensors:
+        raise ValueError("need at least one worker buffer")
+    n = len(host_tensors)
+    h0 = host_tensors[0]
+    dt = _dtype_code(h0)
+    p = h0.numel()
     for h in host_tensors:
-        if h.is_cuda or h.numel() != p or h.dtype != dev_tensors[0].dtype or not h.is_contiguous():
-            raise ValueError("host tensors must be contiguous CPU tensors matching the staging tensors")
+        if h.is_cuda or h.numel() != p or h.dtype != h0.dtype or not h.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors of one dtype and length")
     harr = (ctypes.c_void_p * n)(*[h.data_ptr() for h in host_tensors])
-    _check(load().ra_allreduce_avg_host(harr, arr, n, p, dt, _stream(stream, dev)), "ra_allreduce_avg_host")
+    if dev_tensors is not None:
+        darr, dn, dp, ddt, dev = _rows(dev_tensors)
+        if dn != n or dp != p or ddt != dt:
+            raise ValueError("device staging tensors must match the host tensors")
+    else:
+        darr, dev = None, torch.device("cuda", torch.cuda.current_device())
+    _check(load().ra_allreduce_avg_host(harr, darr, n, p, dt, int(mode), _stream(stream, dev)),
+           "ra_allreduce_avg_host")
 
 
 def ra_chunk_range(p: int, n: int, c: int):

@@ -1,7 +1,6 @@
 // ra_api.cu -- the C ABI (include/ring_allreduce.h): argument checks, the
 // cutting of a request into ring-chunk segments, and kernel dispatch.
 #include <algorithm>
-#include <mutex>
 #include <utility>
 #include <vector>
 
@@ -141,37 +140,6 @@ int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis)
         t += tiles;
     }
     return t;
-}
-
-cudaError_t resident_blocks(const void *kernel, int *out) {
-    struct Entry {
-        int dev;
-        const void *kernel;
-        int blocks;
-    };
-    static std::mutex mu;
-    static std::vector<Entry> cache;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        for (const Entry &x : cache)
-            if (x.dev == dev && x.kernel == kernel) {
-                *out = x.blocks;
-                return cudaSuccess;
-            }
-    }
-    int sms = 0, per_sm = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreadsPerBlock, 0);
-    if (e != cudaSuccess) return e;
-    const int blocks = sms * std::max(per_sm, 1);
-    std::lock_guard<std::mutex> lk(mu);
-    cache.push_back(Entry{dev, kernel, blocks});
-    *out = blocks;
-    return cudaSuccess;
 }
 
 }  // namespace ra
@@ -346,21 +314,49 @@ ra_status ra_allreduce_avg_buckets(void *const *bufs, int n, int dtype, const ra
     return RA_OK;
 }
 
-ra_status ra_allreduce_avg_host(void *const *host_bufs, void *const *dev_bufs, int n, int64_t p, int dtype,
+ra_status ra_allreduce_avg_host(void *const *host_bufs, void *const *dev_bufs, int n, int64_t p, int dtype, int mode,
                                 void *stream) {
-    ra_status st = check_rows(dev_bufs, n, p, dtype);
+    if (n < 1 || n > RA_MAX_N || p < 0 || elem_size(dtype) == 0 || host_bufs == nullptr ||
+        (mode != RA_HOST_AUTO && mode != RA_HOST_DIRECT && mode != RA_HOST_STAGED))
+        return RA_ERR_INVALID_ARG;
+    ra_status st = check_rows(host_bufs, n, p, dtype);
     if (st != RA_OK) return st;
-    if (host_bufs == nullptr) return RA_ERR_INVALID_ARG;
     if (p == 0) return RA_OK;
-    const int esz = elem_size(dtype);
-    for (int k = 0; k < n; ++k) {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(host_bufs[k]);
-        if (a == 0 || a % esz != 0) return RA_ERR_INVALID_ARG;
+    // Direct path: on GB300 the GPU reaches host memory over the coherent
+    // NVLink-C2C link, so the fused kernel can read every worker's host
+    // array and write the mean back in place, with no staging copies.  That
+    // needs a device address for each host array: page-locked (pinned or
+    // registered) memory has one; ordinary pageable memory is usable as is
+    // when the device walks the host page tables.
+    int dev = 0, pageable = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void *direct[RA_MAX_N];
+    bool all_direct = mode != RA_HOST_STAGED;
+    for (int k = 0; k < n && all_direct; ++k) {
+        cudaPointerAttributes a;
+        e = cudaPointerGetAttributes(&a, host_bufs[k]);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr)
+            direct[k] = a.devicePointer;
+        else if (a.type == cudaMemoryTypeUnregistered && pageable)
+            direct[k] = host_bufs[k];
+        else
+            all_direct = false;
     }
+    if (all_direct) return ra_allreduce_avg(direct, n, p, dtype, stream);
+    if (mode == RA_HOST_DIRECT) return RA_ERR_UNSUPPORTED;
+
+    // Staging path: copy in, reduce on the device, copy the mean back.
+    if (dev_bufs == nullptr) return RA_ERR_UNSUPPORTED;
+    st = check_rows(dev_bufs, n, p, dtype);
+    if (st != RA_OK) return st;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t bytes = (size_t)p * esz;
+    const size_t bytes = (size_t)p * elem_size(dtype);
     for (int k = 0; k < n; ++k) {
-        cudaError_t e = cudaMemcpyAsync(dev_bufs[k], host_bufs[k], bytes, cudaMemcpyHostToDevice, s);
+        e = cudaMemcpyAsync(dev_bufs[k], host_bufs[k], bytes, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (n > 1) {
@@ -368,7 +364,7 @@ ra_status ra_allreduce_avg_host(void *const *host_bufs, void *const *dev_bufs, i
         if (st != RA_OK) return st;
     }
     for (int k = 0; k < n; ++k) {
-        cudaError_t e = cudaMemcpyAsync(host_bufs[k], dev_bufs[k], bytes, cudaMemcpyDeviceToHost, s);
+        e = cudaMemcpyAsync(host_bufs[k], dev_bufs[k], bytes, cudaMemcpyDeviceToHost, s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return RA_OK;

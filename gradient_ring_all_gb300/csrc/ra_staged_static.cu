@@ -9,8 +9,8 @@
 // memory on the host (fixed-size tables on the stack).
 //
 // Set-up: the first call on a device (that passes the argument checks) runs,
-// with that device current, cudaGetSymbolAddress on the array and the
-// occupancy queries for the launch size, and caches the results per device.
+// with that device current, cudaGetSymbolAddress on the array and caches the
+// address per device.
 // That first call should therefore come before any stream capture.
 //
 // Sharing: every call on a device uses the same array.  Scatter-reduce
@@ -34,21 +34,11 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
     bool done;
-    float *scratch;   // device address of g_staged_scratch on this device
-    int resident[4];  // resident blocks: [F32 scalar, F32 vector, BF16 scalar, BF16 vector]
+    float *scratch;  // device address of g_staged_scratch on this device
 };
 
 std::mutex g_setup_mu;
 DeviceSetup g_setup[kMaxDevices];
-
-template <class E, bool VEC>
-cudaError_t occupancy(int sms, int *out) {
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, staged_step_kernel<E, VEC>, kThreadsPerBlock, 0);
-    *out = sms * (per_sm > 0 ? per_sm : 1);
-    return e;
-}
 
 // once per device, with that device current
 cudaError_t setup_device(int dev, DeviceSetup *out) {
@@ -58,13 +48,6 @@ cudaError_t setup_device(int dev, DeviceSetup *out) {
         void *addr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&addr, g_staged_scratch);
         if (e != cudaSuccess) return e;
-        int sms = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if ((e = occupancy<F32, false>(sms, &d.resident[0])) != cudaSuccess) return e;
-        if ((e = occupancy<F32, true>(sms, &d.resident[1])) != cudaSuccess) return e;
-        if ((e = occupancy<BF16, false>(sms, &d.resident[2])) != cudaSuccess) return e;
-        if ((e = occupancy<BF16, true>(sms, &d.resident[3])) != cudaSuccess) return e;
         d.scratch = static_cast<float *>(addr);
         d.done = true;
     }
@@ -72,17 +55,17 @@ cudaError_t setup_device(int dev, DeviceSetup *out) {
     return cudaSuccess;
 }
 
+// one tile per block, as for the other staged launches
 template <class E, bool VEC>
-cudaError_t launch_step(const StagedParams &p, int resident, cudaStream_t s) {
-    const int64_t grid = p.ntiles < resident ? p.ntiles : resident;
+cudaError_t launch_step(const StagedParams &p, cudaStream_t s) {
+    const int64_t grid = p.ntiles < kMaxGrid ? p.ntiles : kMaxGrid;
     staged_step_kernel<E, VEC><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_step_any(const StagedParams &p, int dtype, bool vec, const DeviceSetup &d, cudaStream_t s) {
-    if (dtype == RA_F32)
-        return vec ? launch_step<F32, true>(p, d.resident[1], s) : launch_step<F32, false>(p, d.resident[0], s);
-    return vec ? launch_step<BF16, true>(p, d.resident[3], s) : launch_step<BF16, false>(p, d.resident[2], s);
+cudaError_t launch_step_any(const StagedParams &p, int dtype, bool vec, cudaStream_t s) {
+    if (dtype == RA_F32) return vec ? launch_step<F32, true>(p, s) : launch_step<F32, false>(p, s);
+    return vec ? launch_step<BF16, true>(p, s) : launch_step<BF16, false>(p, s);
 }
 
 }  // namespace
@@ -168,17 +151,17 @@ extern "C" ra_status ra_allreduce_avg_staged_static(void *const *bufs, int n, in
     for (int t = 0; t < n - 1 && e == cudaSuccess; ++t) {
         prm.op = kOpScatter;
         prm.t = t;
-        e = launch_step_any(prm, dtype, vec, d, s);
+        e = launch_step_any(prm, dtype, vec, s);
     }
     if (e == cudaSuccess) {
         prm.op = kOpDivide;
         prm.t = 0;
-        e = launch_step_any(prm, dtype, vec, d, s);
+        e = launch_step_any(prm, dtype, vec, s);
     }
     for (int t = 0; t < n - 1 && e == cudaSuccess; ++t) {
         prm.op = kOpGather;
         prm.t = t;
-        e = launch_step_any(prm, dtype, vec, d, s);
+        e = launch_step_any(prm, dtype, vec, s);
     }
     if (e != cudaSuccess) {
         record_cuda_error(e);

@@ -41,7 +41,7 @@
  *     vector path; any other element-aligned pointers take a scalar path
  *     with the same results.
  *   - Every function is thread-safe; the library keeps no state besides
- *     a per-device cache of launch sizes.
+ *     the per-device address of its one built-in scratch array.
  */
 #ifndef RING_ALLREDUCE_H
 #define RING_ALLREDUCE_H
@@ -180,8 +180,8 @@ ra_status ra_allreduce_avg_buckets(void *const *bufs, int n, int dtype, const ra
  * Returns RA_ERR_UNSUPPORTED, before doing anything, when dtype is RA_BF16
  * and p > RA_STAGED_STATIC_MAX_P.
  * The first call on a device (that passes the argument checks) looks up the
- * array's device address and the launch size and caches them; make that
- * first call before any stream capture.  All calls on a device share the
+ * array's device address and caches it; make that first call before any
+ * stream capture.  All calls on a device share the
  * array and it keeps the last call's contents; nothing in it needs clearing
  * (each call writes every partial sum before reading it), but calls whose
  * work overlaps on the GPU race on it: order them on one stream or with
@@ -193,18 +193,28 @@ ra_status ra_allreduce_avg_staged_static(void *const *bufs, int n, int64_t p, in
 
 /*
  * ra_allreduce_avg_host -- ra_allreduce_avg for workers whose gradients
- * live in HOST memory: copies every host array to its device staging
- * buffer, runs the fused all-reduce there, and copies the mean back to
- * every host array, all queued on `stream` (the end-to-end path of a
- * data-parallel step whose gradients start and end on the host).
- *   host_bufs  host array of n HOST pointers, p elements each; page-locked
- *              memory makes the copies asynchronous, pageable memory works
- *              but the CUDA runtime then copies synchronously
+ * live in HOST memory: every host array ends holding the mean (the end-to-end
+ * path of a data-parallel step whose gradients start and end on the host).
+ * Two ways:
+ *   - direct: the device addresses every host array -- page-locked memory
+ *     (cudaHostAlloc / cudaHostRegister), or any host memory on a device
+ *     that walks the host page tables (Grace-Blackwell's coherent
+ *     NVLink-C2C) -- and the fused kernel reads the host arrays and writes
+ *     the mean back to them directly; dev_bufs is not touched;
+ *   - staged: each host array is copied to its device buffer in dev_bufs,
+ *     reduced there, and the mean copied back.
+ *   host_bufs  host array of n HOST pointers, p elements each, not
+ *              overlapping
  *   dev_bufs   host array of n DEVICE pointers, p elements each (caller-owned
- *              staging; they end holding the mean as well)
- * The host arrays must not be read before the stream has finished.
+ *              staging), or NULL
+ *   mode       RA_HOST_AUTO: direct when possible, else staged;
+ *              RA_HOST_DIRECT: direct or RA_ERR_UNSUPPORTED;
+ *              RA_HOST_STAGED: staged (RA_ERR_UNSUPPORTED if dev_bufs is NULL)
+ * All work is queued on `stream`; the host arrays must not be read before
+ * the stream has finished.
  */
-ra_status ra_allreduce_avg_host(void *const *host_bufs, void *const *dev_bufs, int n, int64_t p, int dtype,
+enum { RA_HOST_AUTO = 0, RA_HOST_DIRECT = 1, RA_HOST_STAGED = 2 };
+ra_status ra_allreduce_avg_host(void *const *host_bufs, void *const *dev_bufs, int n, int64_t p, int dtype, int mode,
                                 void *stream);
 
 /* ra_chunk_range -- [begin, end) of chunk c of a p-element array split for
