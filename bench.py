@@ -126,6 +126,60 @@ def _traffic_from_profile(kernel_key: str):
     return None
 
 
+def max_over_ranks(x: float, dist) -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def aggregate_gbs(bytes_per_step: float, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every replica's bytes over the slowest replica's time."""
+    return bytes_per_step * world / (ms_per_step / 1e3) / 1e9
+
+
+def timed_region(step, steps: int, dist, timer):
+    """Barrier, `steps` calls of step(k), barrier; returns (this rank's ms,
+    the max over ranks).  `timer` brackets the region: start(), stop(),
+    sync(), elapsed_ms()."""
+    if dist is not None:
+        dist.barrier()
+    timer.sync()
+    timer.start()
+    for k in range(steps):
+        step(k)
+    timer.stop()
+    timer.sync()
+    if dist is not None:
+        dist.barrier()
+    ms = timer.elapsed_ms()
+    return ms, max_over_ranks(ms, dist)
+
+
+class _CudaEventTimer:
+    def __init__(self, stream):
+        import torch
+        self.torch = torch
+        self.stream = stream
+        self.a = torch.cuda.Event(enable_timing=True)
+        self.b = torch.cuda.Event(enable_timing=True)
+
+    def sync(self):
+        self.torch.cuda.synchronize()
+
+    def start(self):
+        self.a.record(self.stream)
+
+    def stop(self):
+        self.b.record(self.stream)
+
+    def elapsed_ms(self):
+        return self.a.elapsed_time(self.b)
+
+
 def _cpu_oracle_sample(n: int, p: int, reps: int):
     """Time the oracle (as it stands) on a bounded sample: a ring of n workers
     x p elements of the workload's distribution.  Returns (GB/s, seconds)."""
@@ -218,33 +272,21 @@ def run_ours(args):
     # timed region: K launches, an event pair around each on the launch stream
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t_all0 = torch.cuda.Event(enable_timing=True)
-    t_all1 = torch.cuda.Event(enable_timing=True)
     clocks = _ClockSampler(local).start()
     time.sleep(0.3)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    w0 = time.time()
-    t_all0.record(stream)
-    for k in range(args.steps):
+
+    def step(k):
         starts[k].record(stream)
         ra.ra_allreduce_avg(rows, stream)
         ends[k].record(stream)
-    t_all1.record(stream)
-    torch.cuda.synchronize()
+
+    w0 = time.time()
+    _, total_ms = timed_region(step, args.steps, dist, _CudaEventTimer(stream))
     w1 = time.time()
-    if dist:
-        dist.barrier()
     clk = clocks.stop(w0, w1)
-    total_ms = t_all0.elapsed_time(t_all1)
     kern_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if dist:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t[0])
     ms_per_step = total_ms / args.steps
-    value = nbytes * ws / (ms_per_step / 1e3) / 1e9
+    value = aggregate_gbs(nbytes, ws, ms_per_step)
     avg_kernel_ms = sum(kern_ms) / len(kern_ms)
 
     if args.legs == "device":
@@ -268,22 +310,9 @@ def run_ours(args):
 
     def time_host(mode, steps):
         ra.ra_allreduce_avg_host(hrows, rows, mode, stream)  # warm-up
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        if dist:
-            dist.barrier()
-        e0.record(stream)
-        for _ in range(steps):
-            ra.ra_allreduce_avg_host(hrows, rows, mode, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
-        if dist:
-            t = torch.tensor([ms], dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t[0])
-        return ms
+        _, ms = timed_region(lambda k: ra.ra_allreduce_avg_host(hrows, rows, mode, stream), steps, dist,
+                             _CudaEventTimer(stream))
+        return ms / steps
 
     e2e_ms = time_host(ra.RA_HOST_DIRECT, e2e_steps)
     staged_ms = time_host(ra.RA_HOST_STAGED, max(1, e2e_steps // 2))
@@ -314,11 +343,11 @@ def run_ours(args):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "kernel": "fused_allreduce_kernel<F32, N=8>", "avg_launch_ms": avg_kernel_ms,
                      "traffic": _traffic_from_profile("fused_f32_n8_speech300m")},
-        "e2e": {"value": nbytes * ws / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": aggregate_gbs(nbytes, ws, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": n * p * 4, "d2h_bytes_per_step": n * p * 4,
                 "path": "ra_allreduce_avg_host, direct: the fused kernel reads the pinned host rows and "
                         "writes the mean back to every host row over NVLink-C2C"},
-        "e2e_staged": {"value": nbytes * ws / (staged_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": staged_ms,
+        "e2e_staged": {"value": aggregate_gbs(nbytes, ws, staged_ms), "unit": "GB/s", "ms_per_step": staged_ms,
                        "path": "ra_allreduce_avg_host, staged: cudaMemcpyAsync in, fused kernel, cudaMemcpyAsync out"},
         "gpu_launches": args.steps,
         "clocks": clk,

@@ -1,0 +1,82 @@
+"""bench.py's multi-process path on CPU (gloo, world size 2): the barrier +
+max-over-ranks timing of independent replicas, the whole-job aggregate, and
+the reference arm under torchrun (rank 0 alone prints)."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+import time
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+class _WallTimer:
+    def sync(self):
+        pass
+
+    def start(self):
+        self.t0 = time.perf_counter()
+
+    def stop(self):
+        self.t1 = time.perf_counter()
+
+    def elapsed_ms(self):
+        return (self.t1 - self.t0) * 1e3
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    # rank 1 is the slow replica: 4 steps of 30 ms against rank 0's 4 x 5 ms
+    delay = 0.005 if rank == 0 else 0.030
+    mine, slowest = bench.timed_region(lambda k: time.sleep(delay), 4, dist, _WallTimer())
+    q.put((rank, mine, slowest, bench.aggregate_gbs(1e9, world, slowest / 4)))
+    dist.destroy_process_group()
+
+
+def test_replica_timing_takes_the_slowest_rank():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, mine0, max0, val0), (r1, mine1, max1, val1) = res
+    assert max0 == max1 == max(mine0, mine1)
+    assert mine1 >= 120.0 and mine0 < mine1
+    # both replicas' bytes over the slowest replica's time
+    assert abs(val0 - 2 * 1e9 / (max0 / 4 / 1e3) / 1e9) < 1e-9
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
