@@ -70,6 +70,10 @@ def _load():
     lib.oracle_mean_f64.restype = None
     lib.oracle_bucket_plan.argtypes = [vp, i32, i64, i64, vp, vp, i32]
     lib.oracle_bucket_plan.restype = i32
+    lib.oracle_reduce_scatter_avg_bf16.argtypes = [vp, i32, i64]
+    lib.oracle_reduce_scatter_avg_bf16.restype = i32
+    lib.oracle_all_gather.argtypes = [vp, i32, i64, i32]
+    lib.oracle_all_gather.restype = i32
     lib.oracle_ring_traffic.argtypes = [i32, i64, vp, vp]
     lib.oracle_ring_traffic.restype = None
     _lib = lib
@@ -220,3 +224,39 @@ def ring_allreduce_avg_buckets_f32(rows, buckets):
     """Each bucket (offset, count) of the rows is its own ring."""
     for off, cnt in buckets:
         ring_allreduce_avg_f32([r[off:off + cnt] for r in rows])
+
+
+# --------------------------------------------------------------------------
+# the two phases on their own
+
+
+def owned_chunk(n_workers: int, w: int) -> int:
+    """After the scatter-reduce worker w holds the complete chunk w+1."""
+    return (w + 1) % n_workers
+
+
+def reduce_scatter_avg(rows):
+    """Scatter-reduce + owner's division in place; returns {worker: (begin,
+    end)} of the chunk each worker now owns (its only defined result)."""
+    n = len(rows)
+    if rows[0].dtype == np.float32:
+        ring_run_f32(rows, n - 1, True, 0)
+    elif rows[0].dtype == np.uint16:
+        p = _check_rows(rows, np.uint16)
+        if _load().oracle_reduce_scatter_avg_bf16(_row_ptrs(rows), n, p) != 0:
+            raise ValueError("oracle_reduce_scatter_avg_bf16 rejected its arguments")
+    else:
+        raise ValueError("rows must be float32 or bf16 bits")
+    p = rows[0].shape[0]
+    return {w: chunk_range(p, n, owned_chunk(n, w)) for w in range(n)}
+
+
+def all_gather(rows):
+    """Literal all-gather in place (any dtype): worker (c-1) mod N's chunk c
+    reaches every worker."""
+    p = rows[0].shape[0]
+    for r in rows:
+        if r.dtype != rows[0].dtype or r.shape[0] != p or not r.flags.c_contiguous:
+            raise ValueError("rows must be contiguous arrays of one dtype and length")
+    if _load().oracle_all_gather(_row_ptrs(rows), len(rows), p, rows[0].itemsize) != 0:
+        raise ValueError("oracle_all_gather rejected its arguments")

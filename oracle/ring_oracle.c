@@ -351,3 +351,70 @@ uint16_t oracle_ring_avg_point_bf16(const uint16_t *vals, int n_workers, int64_t
         wide[n] = bf16_to_f32(vals[n]);
     return oracle_f32_to_bf16(oracle_ring_avg_point_f32(wide, n_workers, p, i));
 }
+
+/* ------------------------------------------------------------------ */
+/* The two phases on their own ([D] FSDP: gradients are reduce-scattered so
+ * that each GPU keeps the part it owns; parameters are all-gathered before
+ * use; [G] Scatter-Reduce / Allgather).                                 */
+
+/* Reduce-scatter-average of bf16 rows: the scatter-reduce with binary32
+ * partials and the owner's division, as in the full method; afterwards
+ * worker n's chunk n+1 holds the bf16 mean and every other chunk keeps the
+ * worker's input (only the owned chunks are results).                   */
+int oracle_reduce_scatter_avg_bf16(uint16_t *const *rows, int n_workers, int64_t p) {
+    int N = n_workers;
+    if (N < 1 || p < 0)
+        return -1;
+    float **work = (float **)calloc((size_t)N, sizeof(float *));
+    if (!work)
+        return -1;
+    int rc = 0;
+    for (int n = 0; n < N && rc == 0; ++n) {
+        work[n] = (float *)malloc((size_t)(p > 0 ? p : 1) * sizeof(float));
+        if (!work[n])
+            rc = -1;
+        else
+            for (int64_t i = 0; i < p; ++i)
+                work[n][i] = bf16_to_f32(rows[n][i]);
+    }
+    if (rc == 0)
+        rc = oracle_ring_run_f32(work, N, p, N - 1, 1, 1, 0, 0, 0);
+    if (rc == 0)
+        for (int n = 0; n < N; ++n) {
+            int64_t b, e;
+            oracle_chunk_range(p, N, mod_n((int64_t)n + 1, N), &b, &e);
+            for (int64_t i = b; i < e; ++i)
+                rows[n][i] = oracle_f32_to_bf16(work[n][i]); /* exact: bf16 values */
+        }
+    for (int n = 0; n < N; ++n)
+        free(work[n]);
+    free(work);
+    return rc;
+}
+
+/* All-gather of any element type, literally: N-1 iterations in which worker
+ * n sends chunk (n+1-t) mod N to worker n+1, which overwrites its copy.
+ * Starting from worker (c-1) mod N holding chunk c, every worker ends with
+ * every chunk.                                                           */
+int oracle_all_gather(void *const *rows, int n_workers, int64_t p, int elem_bytes) {
+    int N = n_workers;
+    if (N < 1 || p < 0 || elem_bytes < 1)
+        return -1;
+    unsigned char *wire = (unsigned char *)malloc((size_t)(p > 0 ? p : 1) * (size_t)elem_bytes);
+    if (!wire)
+        return -1;
+    for (int t = 0; t < N - 1; ++t) {
+        for (int n = 0; n < N; ++n) {
+            int64_t b, e;
+            oracle_chunk_range(p, N, oracle_gather_send_chunk(N, n, t), &b, &e);
+            memcpy(wire + b * elem_bytes, (unsigned char *)rows[n] + b * elem_bytes, (size_t)(e - b) * elem_bytes);
+        }
+        for (int m = 0; m < N; ++m) {
+            int64_t b, e;
+            oracle_chunk_range(p, N, oracle_gather_recv_chunk(N, m, t), &b, &e);
+            memcpy((unsigned char *)rows[m] + b * elem_bytes, wire + b * elem_bytes, (size_t)(e - b) * elem_bytes);
+        }
+    }
+    free(wire);
+    return 0;
+}

@@ -557,3 +557,69 @@ def test_resnet18_parameter_count():
     numel = synth.shapes.numels(synth.resnet18_shapes())
     assert abs(sum(numel) / 1e6 - f["params_millions"]) < 0.05
     assert abs(sum(numel) * 4 / 1e6 - f["fp32_mb"]) < 0.1
+
+
+# --------------------------------------------------------------------------
+# the two phases on their own ([D] FSDP reduce-scatter / all-gather)
+
+
+@pytest.mark.parametrize("n,p", [(1, 9), (2, 7), (5, 23), (8, 64), (7, 3)])
+def test_reduce_scatter_leaves_each_worker_its_chunk_of_the_mean(n, p):
+    rng = np.random.default_rng(n + 7 * p)
+    g = _int_rows(rng, n, p, lim=2 ** 10)
+    rows = [r.copy() for r in g]
+    owned = oracle.reduce_scatter_avg(rows)
+    for w, (b, e) in owned.items():
+        assert (b, e) == oracle.chunk_range(p, n, (w + 1) % n)
+        for i in range(b, e):
+            assert Fraction(float(rows[w][i])) == X.rn_f32(Fraction(sum(int(r[i]) for r in g), n))
+    # the owners' chunks tile the array exactly once
+    cover = sorted(owned.values())
+    assert sum(e - b for b, e in cover) == p
+
+
+@pytest.mark.parametrize("n", [2, 3, 5, 16])
+def test_reduce_scatter_bf16_owned_chunks_match_the_full_ring(n):
+    import synth
+    p = 4 * n + 3
+    g = [synth.student_t3_bf16(3, w, 1e-3, 0, p) for w in range(n)]
+    full = [r.copy() for r in g]
+    oracle.ring_allreduce_avg_bf16(full)
+    rs = [r.copy() for r in g]
+    owned = oracle.reduce_scatter_avg(rs)
+    for w, (b, e) in owned.items():
+        np.testing.assert_array_equal(rs[w][b:e], full[0][b:e])
+        # outside its chunk a worker keeps its input
+        mask = np.ones(p, bool)
+        mask[b:e] = False
+        np.testing.assert_array_equal(rs[w][mask], g[w][mask])
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.uint16])
+@pytest.mark.parametrize("n,p", [(1, 4), (2, 5), (5, 23), (8, 3)])
+def test_all_gather_spreads_every_owned_chunk(n, p, dtype):
+    # worker (c-1) mod N holds chunk c (marked c+1); everything else is junk
+    rows = [np.full(p, 999, dtype) for _ in range(n)]
+    for c in range(n):
+        b, e = oracle.chunk_range(p, n, c)
+        rows[(c - 1) % n][b:e] = c + 1
+    oracle.all_gather(rows)
+    want = np.empty(p, dtype)
+    for c in range(n):
+        b, e = oracle.chunk_range(p, n, c)
+        want[b:e] = c + 1
+    for r in rows:
+        np.testing.assert_array_equal(r, want)
+
+
+def test_reduce_scatter_then_all_gather_is_the_all_reduce():
+    rng = np.random.default_rng(17)
+    n, p = 6, 1001
+    g = [rng.standard_normal(p).astype(np.float32) for _ in range(n)]
+    full = [r.copy() for r in g]
+    oracle.ring_allreduce_avg_f32(full)
+    rows = [r.copy() for r in g]
+    oracle.reduce_scatter_avg(rows)
+    oracle.all_gather(rows)
+    for r in rows:
+        np.testing.assert_array_equal(r, full[0])
