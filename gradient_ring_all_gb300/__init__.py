@@ -19,7 +19,8 @@ __all__ = [
     "RA_F32", "RA_BF16", "RA_MAX_N", "RaError", "library_path", "load",
     "ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_staged_workspace_bytes",
     "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
-    "RA_STAGED_STATIC_MAX_P", "RA_HOST_AUTO", "RA_HOST_DIRECT", "RA_HOST_STAGED", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
+    "RA_STAGED_STATIC_MAX_P", "RA_HOST_AUTO", "RA_HOST_DIRECT", "RA_HOST_STAGED", "ra_reduce_scatter_avg",
+    "ra_all_gather", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
 ]
 
 RA_F32 = 0
@@ -77,6 +78,8 @@ def load():
     lib.ra_allreduce_avg_buckets.argtypes = [pvp, i32, i32, ctypes.POINTER(_Bucket), i32, vp]
     lib.ra_allreduce_avg_host.argtypes = [pvp, pvp, i32, i64, i32, i32, vp]
     lib.ra_allreduce_avg_staged_static.argtypes = [pvp, i32, i64, i32, ctypes.POINTER(_Traffic), vp]
+    lib.ra_reduce_scatter_avg.argtypes = [pvp, i32, i64, i32, pvp, vp]
+    lib.ra_all_gather.argtypes = [pvp, i32, i64, i32, pvp, vp]
     lib.ra_chunk_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.ra_chunk_range.restype = None
     lib.ra_status_str.argtypes = [i32]
@@ -84,7 +87,7 @@ def load():
     lib.ra_last_cuda_error.argtypes = []
     for nm in ("ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_bucket_plan",
                "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
-               "ra_last_cuda_error"):
+               "ra_reduce_scatter_avg", "ra_all_gather", "ra_last_cuda_error"):
         getattr(lib, nm).restype = i32
     _lib = lib
     return lib
@@ -241,6 +244,38 @@ def ra_allreduce_avg_host(host_tensors, dev_tensors=None, mode=RA_HOST_AUTO, str
         darr, dev = None, torch.device("cuda", torch.cuda.current_device())
     _check(load().ra_allreduce_avg_host(harr, darr, n, p, dt, int(mode), _stream(stream, dev)),
            "ra_allreduce_avg_host")
+
+
+def _shards(shards, tensors, n, p):
+    if shards is None:
+        return None
+    shards = list(shards)
+    if len(shards) != n:
+        raise ValueError("need one shard per worker")
+    for m, sh in enumerate(shards):
+        b, e = ra_chunk_range(p, n, (m + 1) % n)
+        if not sh.is_cuda or sh.dtype != tensors[0].dtype or sh.numel() != e - b or not sh.is_contiguous():
+            raise ValueError("shard %d must be a contiguous CUDA tensor of chunk %d's %d elements"
+                             % (m, (m + 1) % n, e - b))
+    return (ctypes.c_void_p * n)(*[sh.data_ptr() for sh in shards])
+
+
+def ra_reduce_scatter_avg(tensors, shards=None, stream=None) -> None:
+    """Worker (c-1) mod N ends with the mean of chunk c: in place in its own
+    tensor, or in shards[(c-1) mod N] when shards are given."""
+    tensors = list(tensors)
+    arr, n, p, dt, dev = _rows(tensors)
+    sh = _shards(shards, tensors, n, p)
+    _check(load().ra_reduce_scatter_avg(arr, n, p, dt, sh, _stream(stream, dev)), "ra_reduce_scatter_avg")
+
+
+def ra_all_gather(tensors, shards=None, stream=None) -> None:
+    """Chunk c of worker (c-1) mod N (or shards[(c-1) mod N]) is copied into
+    every worker's tensor."""
+    tensors = list(tensors)
+    arr, n, p, dt, dev = _rows(tensors)
+    sh = _shards(shards, tensors, n, p)
+    _check(load().ra_all_gather(arr, n, p, dt, sh, _stream(stream, dev)), "ra_all_gather")
 
 
 def ra_chunk_range(p: int, n: int, c: int):

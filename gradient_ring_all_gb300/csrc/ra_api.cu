@@ -74,9 +74,13 @@ void ring_segments(int64_t off, int64_t count, int n, std::vector<Seg> *out) {
 }
 
 ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, const Seg *segs, int nseg, bool vector,
-                    int mis, cudaStream_t s) {
+                    int mis, cudaStream_t s, void *const *aux = nullptr) {
     FusedLaunch L;
-    for (int k = 0; k < n; ++k) L.rows[k] = bufs[k];
+    for (int k = 0; k < n; ++k) {
+        L.rows[k] = bufs[k];
+        L.aux[k] = aux ? aux[k] : nullptr;
+    }
+    L.out = aux ? 2 : (w ? 1 : 0);
     L.n = n;
     L.dtype = dtype;
     L.w = w;
@@ -90,6 +94,42 @@ ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, con
     if (ntiles == 0) return RA_OK;
     cudaError_t e = dtype == RA_F32 ? launch_fused_f32(L, ntiles, s) : launch_fused_bf16(L, ntiles, s);
     return e == cudaSuccess ? RA_OK : cuda_fail(e);
+}
+
+// Per-chunk base addresses for the shard calls: element i of chunk c lives at
+// base[c] + i * esz -- the owning worker's own array, or its shard buffer
+// shifted back by the chunk's first index.  Checks the shards (non-null,
+// aligned, disjoint from each other and from the rows) and whether the
+// vector path still applies.
+ra_status shard_bases(void *const *bufs, int n, int64_t p, int dtype, void *const *shards, void **base,
+                      bool *vector, int mis) {
+    const int esz = elem_size(dtype), V = vec_elems(dtype);
+    std::vector<std::pair<uintptr_t, uintptr_t>> r;
+    if (shards) {
+        for (int k = 0; k < n; ++k) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(bufs[k]);
+            r.emplace_back(a, a + (uintptr_t)p * esz);
+        }
+    }
+    for (int c = 0; c < n; ++c) {
+        const int owner = (c + n - 1) % n;
+        int64_t b, e;
+        chunk_of(p, n, c, &b, &e);
+        if (!shards) {
+            base[c] = bufs[owner];
+            continue;
+        }
+        const uintptr_t a = reinterpret_cast<uintptr_t>(shards[owner]);
+        if (e > b) {
+            if (a == 0 || a % esz != 0) return RA_ERR_INVALID_ARG;
+            r.emplace_back(a, a + (uintptr_t)(e - b) * esz);
+        }
+        const uintptr_t shifted = a - (uintptr_t)b * esz;  // never dereferenced below index b
+        base[c] = reinterpret_cast<void *>(shifted);
+        if (e > b && (int)((shifted / esz) % V) != mis) *vector = false;
+    }
+    if (shards && !ranges_disjoint(std::move(r))) return RA_ERR_OVERLAP;
+    return RA_OK;
 }
 
 }  // namespace
@@ -368,6 +408,42 @@ ra_status ra_allreduce_avg_host(void *const *host_bufs, void *const *dev_bufs, i
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return RA_OK;
+}
+
+ra_status ra_reduce_scatter_avg(void *const *bufs, int n, int64_t p, int dtype, void *const *shards, void *stream) {
+    ra_status st = check_rows(bufs, n, p, dtype);
+    if (st != RA_OK || p == 0 || (n == 1 && shards == nullptr)) return st;
+    int mis = 0;
+    bool vector = common_misalignment(bufs, n, dtype, &mis);
+    void *base[RA_MAX_N];
+    st = shard_bases(bufs, n, p, dtype, shards, base, &vector, mis);
+    if (st != RA_OK) return st;
+    std::vector<Seg> segs;
+    ring_segments(0, p, n, &segs);
+    return run_fused(bufs, n, dtype, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
+                     static_cast<cudaStream_t>(stream), base);
+}
+
+ra_status ra_all_gather(void *const *bufs, int n, int64_t p, int dtype, void *const *shards, void *stream) {
+    ra_status st = check_rows(bufs, n, p, dtype);
+    if (st != RA_OK || p == 0 || (n == 1 && shards == nullptr)) return st;
+    GatherLaunch L;
+    for (int k = 0; k < n; ++k) L.rows[k] = bufs[k];
+    L.n = n;
+    L.dtype = dtype;
+    int mis = 0;
+    L.vector = common_misalignment(bufs, n, dtype, &mis);
+    L.mis = mis;
+    L.skip_owner = shards == nullptr;
+    st = shard_bases(bufs, n, p, dtype, shards, L.src, &L.vector, mis);
+    if (st != RA_OK) return st;
+    std::vector<Seg> segs;
+    ring_segments(0, p, n, &segs);
+    L.ntiles = staged_assign_tiles(segs.data(), (int)segs.size(), dtype, L.vector, mis);
+    L.seg = segs.data();
+    L.nseg = (int)segs.size();
+    cudaError_t e = launch_all_gather(L, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RA_OK : cuda_fail(e);
 }
 
 void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end) {

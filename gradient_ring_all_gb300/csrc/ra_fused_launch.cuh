@@ -9,11 +9,14 @@
 
 namespace ra {
 
-template <class E, int NT, bool SGD, bool VEC, int MAXSEG>
+template <class E, int NT, int OUT, bool VEC, int MAXSEG>
 static cudaError_t fused_launch_one(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     FusedParams<MAXSEG> p;
     memset(&p, 0, sizeof(p));
-    for (int k = 0; k < L.n; ++k) p.rows[k] = L.rows[k];
+    for (int k = 0; k < L.n; ++k) {
+        p.rows[k] = L.rows[k];
+        p.aux[k] = L.aux[k];
+    }
     p.w = L.w;
     p.lr = L.lr;
     p.n = L.n;
@@ -28,24 +31,25 @@ static cudaError_t fused_launch_one(const FusedLaunch &L, int64_t ntiles, cudaSt
     // 6.28 TB/s at N=8, P=300M f32).  The kernel's tile loop only matters
     // past 2^31-1 tiles.
     const int64_t grid = ntiles < kMaxGrid ? ntiles : kMaxGrid;
-    fused_allreduce_kernel<E, NT, SGD, VEC, MAXSEG><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    fused_allreduce_kernel<E, NT, OUT, VEC, MAXSEG><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 
 template <class E, int NT>
 static cudaError_t fused_launch_nt(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
-    const bool sgd = L.w != nullptr;
     const bool big = L.nseg > kSegSmall;
-    if (sgd && big) return cudaErrorInvalidValue;  // the SGD call has at most n segments
+    if (L.out != kOutAll && big) return cudaErrorInvalidValue;  // SGD / reduce-scatter use n segments
     if (L.vector) {
-        if (sgd) return fused_launch_one<E, NT, true, true, kSegSmall>(L, ntiles, s);
-        if (big) return fused_launch_one<E, NT, false, true, kSegLarge>(L, ntiles, s);
-        return fused_launch_one<E, NT, false, true, kSegSmall>(L, ntiles, s);
+        if (L.out == kOutAllSgd) return fused_launch_one<E, NT, kOutAllSgd, true, kSegSmall>(L, ntiles, s);
+        if (L.out == kOutOne) return fused_launch_one<E, NT, kOutOne, true, kSegSmall>(L, ntiles, s);
+        if (big) return fused_launch_one<E, NT, kOutAll, true, kSegLarge>(L, ntiles, s);
+        return fused_launch_one<E, NT, kOutAll, true, kSegSmall>(L, ntiles, s);
     }
     // scalar path: generic worker count only
-    if (sgd) return fused_launch_one<E, 0, true, false, kSegSmall>(L, ntiles, s);
-    if (big) return fused_launch_one<E, 0, false, false, kSegLarge>(L, ntiles, s);
-    return fused_launch_one<E, 0, false, false, kSegSmall>(L, ntiles, s);
+    if (L.out == kOutAllSgd) return fused_launch_one<E, 0, kOutAllSgd, false, kSegSmall>(L, ntiles, s);
+    if (L.out == kOutOne) return fused_launch_one<E, 0, kOutOne, false, kSegSmall>(L, ntiles, s);
+    if (big) return fused_launch_one<E, 0, kOutAll, false, kSegLarge>(L, ntiles, s);
+    return fused_launch_one<E, 0, kOutAll, false, kSegSmall>(L, ntiles, s);
 }
 
 template <class E>

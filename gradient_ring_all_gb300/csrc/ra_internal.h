@@ -59,9 +59,11 @@ enum StagedOp { kOpScatter = 0, kOpDivide = 1, kOpGather = 2 };
 
 struct FusedLaunch {
     void *rows[RA_MAX_N];
+    void *aux[RA_MAX_N];  // reduce-scatter: destination base per chunk
+    int out;              // 0: all workers, 1: all workers + SGD, 2: one destination per chunk
     int n;
     int dtype;
-    float *w;  // null: plain average
+    float *w;  // SGD weights
     float lr;
     bool vector;
     int mis;
@@ -90,6 +92,20 @@ struct StagedLaunch {
     int64_t ntiles;
 };
 cudaError_t launch_staged_step(const StagedLaunch &L, int op, int t, cudaStream_t s);
+
+struct GatherLaunch {
+    void *rows[RA_MAX_N];
+    void *src[RA_MAX_N];  // source base per chunk
+    int n;
+    int dtype;
+    bool vector;
+    int mis;
+    bool skip_owner;
+    const Seg *seg;
+    int nseg;
+    int64_t ntiles;
+};
+cudaError_t launch_all_gather(const GatherLaunch &L, cudaStream_t s);
 
 int fused_compile_time_n(int n);  // the specialised worker count used for n (0 = generic)
 

@@ -137,9 +137,15 @@ __device__ __forceinline__ int ring_idx(int c, int k, int n) {
 // ---------------------------------------------------------------------------
 // segment table
 
+// Where the fused kernel puts the mean: every worker's array (all-reduce),
+// the same plus the SGD step, or one destination per chunk (reduce-scatter:
+// the worker that owns the chunk, or a separate shard buffer).
+enum FusedOut { kOutAll = 0, kOutAllSgd = 1, kOutOne = 2 };
+
 template <int MAXSEG>
 struct FusedParams {
     void *rows[RA_MAX_N];  // worker arrays (device)
+    void *aux[RA_MAX_N];   // kOutOne: element i of chunk c goes to aux[c] + i * element size
     float *w;              // SGD weights (device) or null
     float lr;
     int n;                 // workers
@@ -167,19 +173,55 @@ __device__ __forceinline__ int find_seg(const Seg *seg, int nseg, int64_t tile) 
 // fused kernel
 
 // one element through the scalar path: ring-order fold from worker c
-template <class E, int NT, bool SGD, int MAXSEG>
+template <class E, int NT, int OUT, int MAXSEG>
 __device__ __forceinline__ void fused_scalar(const FusedParams<MAXSEG> &p, int c, int64_t i) {
     const int n = NT > 0 ? NT : p.n;
     float acc = load_scalar<E>(p.rows[c], i);
     for (int k = 1; k < n; ++k) acc = __fadd_rn(load_scalar<E>(p.rows[ring_idx(c, k, n)], i), acc);
     const float avg = div_n<NT>(acc, n);
-    const float held = store_scalar_all<E>(p.rows, n, i, avg);
-    if (SGD) p.w[i] = __fsub_rn(p.w[i], __fmul_rn(p.lr, held));
+    if constexpr (OUT == kOutOne) {
+        store_scalar_all<E>(&p.aux[c], 1, i, avg);
+    } else {
+        const float held = store_scalar_all<E>(p.rows, n, i, avg);
+        if constexpr (OUT == kOutAllSgd) p.w[i] = __fsub_rn(p.w[i], __fmul_rn(p.lr, held));
+    }
 }
 
 constexpr int kThreads = kThreadsPerBlock;
 
-template <class E, int NT, bool SGD, int MAXSEG>
+// store one vector of means (and apply the SGD step to the matching weights)
+template <class E, int NT, int OUT, int MAXSEG>
+__device__ __forceinline__ void fused_emit(const FusedParams<MAXSEG> &p, int c, int n, int64_t i,
+                                           const float (&avg)[E::kVec]) {
+    constexpr int V = E::kVec;
+    constexpr int esz = (int)sizeof(typename E::T);
+    float held[V];
+    const uint4 out = pack<E>(avg, held);
+    if constexpr (OUT == kOutOne) {
+        st_vec(reinterpret_cast<char *>(p.aux[c]) + i * esz, out);
+    } else {
+        if constexpr (NT > 0) {
+#pragma unroll
+            for (int k = 0; k < NT; ++k) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, out);
+        } else {
+            for (int k = 0; k < n; ++k) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, out);
+        }
+        if constexpr (OUT == kOutAllSgd) {
+#pragma unroll
+            for (int e = 0; e < V; e += 4) {
+                float4 *wp = reinterpret_cast<float4 *>(p.w + i + e);
+                float4 wv = __ldcs(wp);
+                wv.x = __fsub_rn(wv.x, __fmul_rn(p.lr, held[e + 0]));
+                wv.y = __fsub_rn(wv.y, __fmul_rn(p.lr, held[e + 1]));
+                wv.z = __fsub_rn(wv.z, __fmul_rn(p.lr, held[e + 2]));
+                wv.w = __fsub_rn(wv.w, __fmul_rn(p.lr, held[e + 3]));
+                __stcs(wp, wv);
+            }
+        }
+    }
+}
+
+template <class E, int NT, int OUT, int MAXSEG>
 __device__ __forceinline__ void fused_vectors(const FusedParams<MAXSEG> &p, int c, int64_t i0, int64_t ae) {
     constexpr int V = E::kVec;
     constexpr int VPT = fused_vec_per_thread(NT);
@@ -210,24 +252,10 @@ __device__ __forceinline__ void fused_vectors(const FusedParams<MAXSEG> &p, int 
 #pragma unroll
                     for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(t[e], acc[e]);
                 }
-                float avg[V], held[V];
+                float avg[V];
 #pragma unroll
                 for (int e = 0; e < V; ++e) avg[e] = div_n<NT>(acc[e], n);
-                const uint4 out = pack<E>(avg, held);
-#pragma unroll
-                for (int k = 0; k < NT; ++k) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, out);
-                if constexpr (SGD) {
-#pragma unroll
-                    for (int e = 0; e < V; e += 4) {
-                        float4 *wp = reinterpret_cast<float4 *>(p.w + i + e);
-                        float4 wv = __ldcs(wp);
-                        wv.x = __fsub_rn(wv.x, __fmul_rn(p.lr, held[e + 0]));
-                        wv.y = __fsub_rn(wv.y, __fmul_rn(p.lr, held[e + 1]));
-                        wv.z = __fsub_rn(wv.z, __fmul_rn(p.lr, held[e + 2]));
-                        wv.w = __fsub_rn(wv.w, __fmul_rn(p.lr, held[e + 3]));
-                        __stcs(wp, wv);
-                    }
-                }
+                fused_emit<E, NT, OUT>(p, c, n, i, avg);
             }
         }
     } else {
@@ -255,29 +283,16 @@ __device__ __forceinline__ void fused_vectors(const FusedParams<MAXSEG> &p, int 
                 }
             }
         }
-        float avg[V], held[V];
+        float avg[V];
 #pragma unroll
         for (int e = 0; e < V; ++e) avg[e] = div_n<0>(acc[e], n);
-        const uint4 out = pack<E>(avg, held);
-        for (int k = 0; k < n; ++k) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, out);
-        if constexpr (SGD) {
-#pragma unroll
-            for (int e = 0; e < V; e += 4) {
-                float4 *wp = reinterpret_cast<float4 *>(p.w + i + e);
-                float4 wv = __ldcs(wp);
-                wv.x = __fsub_rn(wv.x, __fmul_rn(p.lr, held[e + 0]));
-                wv.y = __fsub_rn(wv.y, __fmul_rn(p.lr, held[e + 1]));
-                wv.z = __fsub_rn(wv.z, __fmul_rn(p.lr, held[e + 2]));
-                wv.w = __fsub_rn(wv.w, __fmul_rn(p.lr, held[e + 3]));
-                __stcs(wp, wv);
-            }
-        }
+        fused_emit<E, 0, OUT>(p, c, n, i, avg);
     }
 }
 
 // VECTOR: rows share their 16-byte misalignment (vector interior + scalar
 // edges); otherwise every element takes the scalar path.
-template <class E, int NT, bool SGD, bool VECTOR, int MAXSEG>
+template <class E, int NT, int OUT, bool VECTOR, int MAXSEG>
 __global__ void __launch_bounds__(kThreads) fused_allreduce_kernel(const __grid_constant__ FusedParams<MAXSEG> p) {
     constexpr int V = E::kVec;
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
@@ -289,16 +304,16 @@ __global__ void __launch_bounds__(kThreads) fused_allreduce_kernel(const __grid_
             int64_t ab, ae;
             vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
             const int64_t i0 = ab + (t_in_seg * fused_tile_vectors(NT) + threadIdx.x) * V;
-            fused_vectors<E, NT, SGD>(p, c, i0, ae);
-            if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) fused_scalar<E, NT, SGD>(p, c, sg.begin + threadIdx.x);
+            fused_vectors<E, NT, OUT>(p, c, i0, ae);
+            if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) fused_scalar<E, NT, OUT>(p, c, sg.begin + threadIdx.x);
             const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
-            if (last && threadIdx.x < sg.end - ae) fused_scalar<E, NT, SGD>(p, c, ae + threadIdx.x);
+            if (last && threadIdx.x < sg.end - ae) fused_scalar<E, NT, OUT>(p, c, ae + threadIdx.x);
         } else {
             const int64_t i0 = sg.begin + t_in_seg * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
 #pragma unroll 4
             for (int j = 0; j < kScalarPerThread; ++j) {
                 const int64_t i = i0 + (int64_t)j * kThreads;
-                if (i < sg.end) fused_scalar<E, NT, SGD>(p, c, i);
+                if (i < sg.end) fused_scalar<E, NT, OUT>(p, c, i);
             }
         }
     }
@@ -447,6 +462,72 @@ __global__ void __launch_bounds__(kThreads) staged_step_kernel(const __grid_cons
             for (int j = 0; j < kScalarPerThread; ++j) {
                 const int64_t i = i0 + (int64_t)j * kThreads;
                 if (i < sg.end) staged_scalar<E>(p, sg.c, i);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// all-gather kernel: chunk c travels from the worker that owns it, worker
+// (c - 1) mod n (or from a separate shard buffer), to every worker (Gibiansky,
+// "Allgather": the received chunk overwrites the receiver's copy).
+
+struct GatherParams {
+    void *rows[RA_MAX_N];
+    void *src[RA_MAX_N];  // element i of chunk c is read at src[c] + i * element size
+    int n;
+    int nseg;
+    int mis;
+    int skip_owner;       // 1: the source is the owner's own array, which is not rewritten
+    int64_t ntiles;
+    Seg seg[RA_MAX_N];
+};
+
+template <class E>
+__device__ __forceinline__ void gather_scalar(const GatherParams &p, int c, int64_t i) {
+    using T = typename E::T;
+    const T v = reinterpret_cast<const T *>(p.src[c])[i];
+    const int owner = c == 0 ? p.n - 1 : c - 1;
+    for (int k = 0; k < p.n; ++k)
+        if (!(p.skip_owner && k == owner)) reinterpret_cast<T *>(p.rows[k])[i] = v;
+}
+
+template <class E, bool VEC>
+__global__ void __launch_bounds__(kThreads) all_gather_kernel(const __grid_constant__ GatherParams p) {
+    constexpr int V = E::kVec;
+    constexpr int esz = (int)sizeof(typename E::T);
+    for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+        const int s = find_seg<RA_MAX_N>(p.seg, p.nseg, tile);
+        const Seg sg = p.seg[s];
+        const int c = sg.c;
+        const int owner = c == 0 ? p.n - 1 : c - 1;
+        const int64_t t_in_seg = tile - sg.tile0;
+        if constexpr (VEC) {
+            int64_t ab, ae;
+            vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
+            const int64_t i0 = ab + (t_in_seg * kStagedTileVec + threadIdx.x) * V;
+            constexpr int J = kStagedTileVec / kThreads;
+            uint4 v[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int64_t i = i0 + (int64_t)j * kThreads * V;
+                if (i < ae) v[j] = ld_vec(reinterpret_cast<const char *>(p.src[c]) + i * esz);
+            }
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int64_t i = i0 + (int64_t)j * kThreads * V;
+                if (i < ae)
+                    for (int k = 0; k < p.n; ++k)
+                        if (!(p.skip_owner && k == owner)) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, v[j]);
+            }
+            if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) gather_scalar<E>(p, c, sg.begin + threadIdx.x);
+            const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
+            if (last && threadIdx.x < sg.end - ae) gather_scalar<E>(p, c, ae + threadIdx.x);
+        } else {
+            const int64_t i0 = sg.begin + t_in_seg * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
+            for (int j = 0; j < kScalarPerThread; ++j) {
+                const int64_t i = i0 + (int64_t)j * kThreads;
+                if (i < sg.end) gather_scalar<E>(p, c, i);
             }
         }
     }

@@ -31,4 +31,30 @@ cudaError_t launch_staged_step(const StagedLaunch &L, int op, int t, cudaStream_
     return L.vector ? staged_launch_one<BF16, true>(L, op, t, s) : staged_launch_one<BF16, false>(L, op, t, s);
 }
 
+template <class E, bool VEC>
+static cudaError_t gather_launch_one(const GatherLaunch &L, cudaStream_t s) {
+    GatherParams p;
+    memset(&p, 0, sizeof(p));
+    for (int k = 0; k < L.n; ++k) {
+        p.rows[k] = L.rows[k];
+        p.src[k] = L.src[k];
+    }
+    p.n = L.n;
+    p.nseg = L.nseg;
+    p.mis = L.mis;
+    p.skip_owner = L.skip_owner ? 1 : 0;
+    p.ntiles = L.ntiles;
+    for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
+    const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
+    all_gather_kernel<E, VEC><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_all_gather(const GatherLaunch &L, cudaStream_t s) {
+    if (L.nseg > RA_MAX_N) return cudaErrorInvalidValue;
+    if (L.dtype == RA_F32)
+        return L.vector ? gather_launch_one<F32, true>(L, s) : gather_launch_one<F32, false>(L, s);
+    return L.vector ? gather_launch_one<BF16, true>(L, s) : gather_launch_one<BF16, false>(L, s);
+}
+
 }  // namespace ra

@@ -217,6 +217,36 @@ enum { RA_HOST_AUTO = 0, RA_HOST_DIRECT = 1, RA_HOST_STAGED = 2 };
 ra_status ra_allreduce_avg_host(void *const *host_bufs, void *const *dev_bufs, int n, int64_t p, int dtype, int mode,
                                 void *stream);
 
+/*
+ * ra_reduce_scatter_avg -- the scatter-reduce half of the ring on its own,
+ * with the owner's division: afterwards the worker that holds the complete
+ * chunk c, worker (c - 1) mod n, has the mean of chunk c (Gibiansky,
+ * "Scatter-Reduce": each GPU ends with one chunk of the final result;
+ * "[PyTorch] GPU 분산 학습 1 - DP / DDP / FSDP 개념", FSDP: the gradients are
+ * reduce-scattered so each GPU keeps the part it updates).  Same summation
+ * order and rounding as ra_allreduce_avg.  One fused pass: N*P reads, P
+ * writes.
+ *   shards  NULL: the mean of chunk c is written into bufs[(c-1) mod n] at
+ *           chunk c's elements; every other element keeps its input.
+ *           Otherwise a host array of n DEVICE pointers: shards[m] receives
+ *           the mean of chunk (m+1) mod n (ra_chunk_range gives its length);
+ *           bufs are not written.  Shards must not overlap each other or
+ *           the worker arrays.
+ */
+ra_status ra_reduce_scatter_avg(void *const *bufs, int n, int64_t p, int dtype, void *const *shards, void *stream);
+
+/*
+ * ra_all_gather -- the all-gather half of the ring on its own: chunk c,
+ * held by worker (c - 1) mod n, is copied to every worker (Gibiansky,
+ * "Allgather": received chunks overwrite; FSDP: the parameter shards are
+ * all-gathered before a layer runs).  P reads, (N-1)*P writes in place.
+ *   shards  NULL: the source of chunk c is bufs[(c-1) mod n] at chunk c's
+ *           elements, and the other n-1 workers' chunk c is overwritten.
+ *           Otherwise a host array of n DEVICE pointers: shards[m] holds
+ *           chunk (m+1) mod n, which is written to every worker's array.
+ */
+ra_status ra_all_gather(void *const *bufs, int n, int64_t p, int dtype, void *const *shards, void *stream);
+
 /* ra_chunk_range -- [begin, end) of chunk c of a p-element array split for
  * n workers (the first p mod n chunks hold one extra element). */
 void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end);
