@@ -74,6 +74,11 @@ def _load():
     lib.oracle_reduce_scatter_avg_bf16.restype = i32
     lib.oracle_all_gather.argtypes = [vp, i32, i64, i32]
     lib.oracle_all_gather.restype = i32
+    lib.oracle_ring_allreduce_avg_bf16_wire.argtypes = [vp, i32, i64]
+    lib.oracle_ring_allreduce_avg_bf16_wire.restype = i32
+    for nm in ("oracle_single_reducer_avg_f32", "oracle_single_reducer_avg_bf16"):
+        getattr(lib, nm).argtypes = [vp, i32, i64, vp, vp]
+        getattr(lib, nm).restype = i32
     lib.oracle_ring_traffic.argtypes = [i32, i64, vp, vp]
     lib.oracle_ring_traffic.restype = None
     _lib = lib
@@ -260,3 +265,31 @@ def all_gather(rows):
             raise ValueError("rows must be contiguous arrays of one dtype and length")
     if _load().oracle_all_gather(_row_ptrs(rows), len(rows), p, rows[0].itemsize) != 0:
         raise ValueError("oracle_all_gather rejected its arguments")
+
+
+# --------------------------------------------------------------------------
+# variants: bf16 partials on the wire, and the single reducer
+
+
+def ring_allreduce_avg_bf16_wire(rows):
+    """The ring over bf16 arrays: every partial sum rounded to bf16 (in place)."""
+    p = _check_rows(rows, np.uint16)
+    if _load().oracle_ring_allreduce_avg_bf16_wire(_row_ptrs(rows), len(rows), p) != 0:
+        raise ValueError("oracle_ring_allreduce_avg_bf16_wire rejected its arguments")
+
+
+def single_reducer_avg(rows):
+    """Worker 0 sums the others' arrays in worker order, divides, broadcasts
+    (in place); returns per-worker (sent, received) element counts."""
+    n = len(rows)
+    sent = np.zeros(n, np.int64)
+    recv = np.zeros(n, np.int64)
+    if rows[0].dtype == np.float32:
+        p = _check_rows(rows, np.float32)
+        rc = _load().oracle_single_reducer_avg_f32(_row_ptrs(rows), n, p, _ptr(sent), _ptr(recv))
+    else:
+        p = _check_rows(rows, np.uint16)
+        rc = _load().oracle_single_reducer_avg_bf16(_row_ptrs(rows), n, p, _ptr(sent), _ptr(recv))
+    if rc != 0:
+        raise ValueError("oracle single reducer rejected its arguments")
+    return sent, recv

@@ -418,3 +418,110 @@ int oracle_all_gather(void *const *rows, int n_workers, int64_t p, int elem_byte
     free(wire);
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* bf16 on the wire: the literal ring over bf16 arrays.  A receiver widens
+ * its own value and the received partial to binary32, adds them, and stores
+ * the sum back into its bf16 array (rounded to nearest even), so every
+ * partial sum is a bf16 number; the owner divides its bf16 sum by N in
+ * binary32 and rounds the mean to bf16.  ([G] Scatter-Reduce with the
+ * arrays kept in bf16.)                                                  */
+int oracle_ring_allreduce_avg_bf16_wire(uint16_t *const *rows, int n_workers, int64_t p) {
+    int N = n_workers;
+    if (N < 1 || p < 0)
+        return -1;
+    uint16_t *wire = (uint16_t *)malloc((size_t)(p > 0 ? p : 1) * sizeof(uint16_t));
+    if (!wire)
+        return -1;
+    for (int t = 0; t < N - 1; ++t) {
+        for (int n = 0; n < N; ++n) {
+            int64_t b, e;
+            oracle_chunk_range(p, N, oracle_scatter_send_chunk(N, n, t), &b, &e);
+            for (int64_t i = b; i < e; ++i)
+                wire[i] = rows[n][i];
+        }
+        for (int m = 0; m < N; ++m) {
+            int64_t b, e;
+            oracle_chunk_range(p, N, oracle_scatter_recv_chunk(N, m, t), &b, &e);
+            for (int64_t i = b; i < e; ++i) {
+                float sum = bf16_to_f32(rows[m][i]) + bf16_to_f32(wire[i]);
+                rows[m][i] = oracle_f32_to_bf16(sum);
+            }
+        }
+    }
+    float fn = (float)N;
+    for (int n = 0; n < N; ++n) {
+        int64_t b, e;
+        oracle_chunk_range(p, N, mod_n((int64_t)n + 1, N), &b, &e);
+        for (int64_t i = b; i < e; ++i)
+            rows[n][i] = oracle_f32_to_bf16(bf16_to_f32(rows[n][i]) / fn);
+    }
+    free(wire);
+    return oracle_all_gather((void *const *)rows, N, p, 2);
+}
+
+/* ------------------------------------------------------------------ */
+/* The single reducer ([G] The Communication Problem: every GPU sends its
+ * gradient to one GPU, which averages them and sends the average back to
+ * all).  Reading: worker 0 is the reducer; it receives the other workers'
+ * arrays in worker order 1, 2, ..., N-1 and adds each to its running sum
+ * (own + received), divides by N, and sends the mean to every other worker.
+ * Binary32 rows; sent / received count elements per worker.              */
+int oracle_single_reducer_avg_f32(float *const *rows, int n_workers, int64_t p, int64_t *sent, int64_t *received) {
+    int N = n_workers;
+    if (N < 1 || p < 0)
+        return -1;
+    for (int m = 1; m < N; ++m) {
+        for (int64_t i = 0; i < p; ++i)
+            rows[0][i] = rows[0][i] + rows[m][i];
+        if (sent)
+            sent[m] += p;
+        if (received)
+            received[0] += p;
+    }
+    float fn = (float)N;
+    for (int64_t i = 0; i < p; ++i)
+        rows[0][i] = rows[0][i] / fn;
+    for (int m = 1; m < N; ++m) {
+        memcpy(rows[m], rows[0], (size_t)p * sizeof(float));
+        if (sent)
+            sent[0] += p;
+        if (received)
+            received[m] += p;
+    }
+    return 0;
+}
+
+/* The same with bf16 arrays: widened exactly, binary32 running sum, the
+ * mean rounded to bf16 once.                                             */
+int oracle_single_reducer_avg_bf16(uint16_t *const *rows, int n_workers, int64_t p, int64_t *sent,
+                                   int64_t *received) {
+    int N = n_workers;
+    if (N < 1 || p < 0)
+        return -1;
+    float *acc = (float *)malloc((size_t)(p > 0 ? p : 1) * sizeof(float));
+    if (!acc)
+        return -1;
+    for (int64_t i = 0; i < p; ++i)
+        acc[i] = bf16_to_f32(rows[0][i]);
+    for (int m = 1; m < N; ++m) {
+        for (int64_t i = 0; i < p; ++i)
+            acc[i] = acc[i] + bf16_to_f32(rows[m][i]);
+        if (sent)
+            sent[m] += p;
+        if (received)
+            received[0] += p;
+    }
+    float fn = (float)N;
+    for (int64_t i = 0; i < p; ++i)
+        rows[0][i] = oracle_f32_to_bf16(acc[i] / fn);
+    for (int m = 1; m < N; ++m) {
+        memcpy(rows[m], rows[0], (size_t)p * sizeof(uint16_t));
+        if (sent)
+            sent[0] += p;
+        if (received)
+            received[m] += p;
+    }
+    free(acc);
+    return 0;
+}

@@ -623,3 +623,97 @@ def test_reduce_scatter_then_all_gather_is_the_all_reduce():
     oracle.all_gather(rows)
     for r in rows:
         np.testing.assert_array_equal(r, full[0])
+
+
+# --------------------------------------------------------------------------
+# bf16 on the wire
+
+
+def _bf16_fold(vals, start):
+    """Left fold from `start` with every partial rounded: fp32 add, then bf16."""
+    n = len(vals)
+    acc = X.bf16_value(vals[start])
+    for k in range(1, n):
+        acc = X.rn_bf16(X.rn_f32(X.bf16_value(vals[(start + k) % n]) + acc))
+    return acc
+
+
+@pytest.mark.parametrize("n,p", [(2, 9), (3, 20), (5, 101), (16, 333)])
+def test_bf16_wire_rounds_every_partial(n, p):
+    import synth
+    g = [synth.student_t3_bf16(3, w, 1e-3, 0, p) for w in range(n)]
+    rows = [r.copy() for r in g]
+    oracle.ring_allreduce_avg_bf16_wire(rows)
+    for c in range(n):
+        b, e = oracle.chunk_range(p, n, c)
+        for i in range(b, e):
+            want = X.rn_bf16(X.rn_f32(_bf16_fold([r[i] for r in g], c) / n))
+            for r in rows:
+                assert X.bf16_value(r[i]) == want
+
+
+def test_bf16_wire_loses_what_binary32_partials_keep():
+    # 256 + 1 + 1 over 3 workers: with bf16 partials 256 + 1 rounds back to
+    # 256 (ties to even), so the mean is bf16(256 / 3) = 85.5; binary32
+    # partials give 258 / 3 = 86.
+    b = [np.array([np.float32(v).view(np.uint32) >> 16], np.uint16) for v in (256.0, 1.0, 1.0)]
+    wire = [r.copy() for r in b]
+    oracle.ring_allreduce_avg_bf16_wire(wire)
+    assert X.bf16_value(wire[0][0]) == Fraction(171, 2)
+    f32 = [r.copy() for r in b]
+    oracle.ring_allreduce_avg_bf16(f32)
+    assert X.bf16_value(f32[0][0]) == 86
+
+
+@pytest.mark.parametrize("n", [2, 4, 7])
+def test_bf16_wire_exact_when_partials_fit(n):
+    # integers |v| <= 16 over at most 7 workers: every partial fits bf16
+    rng = np.random.default_rng(n)
+    p = 3 * n + 1
+    vals, rows = _bf16_rows_from_ints(rng, n, p, 16)
+    oracle.ring_allreduce_avg_bf16_wire(rows)
+    for i in range(p):
+        s = sum(int(v[i]) for v in vals)
+        assert X.bf16_value(rows[0][i]) == X.rn_bf16(X.rn_f32(Fraction(s, n)))
+
+
+# --------------------------------------------------------------------------
+# single reducer ([G] The Communication Problem)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 8, 13])
+def test_single_reducer_folds_in_worker_order(n):
+    rng = np.random.default_rng(40 + n)
+    p = 50
+    choices = np.array([2.0 ** 24, -2.0 ** 24, 1.0, 3.0, -1.0, 0.5], np.float32)
+    g = [choices[rng.integers(0, choices.size, p)] for _ in range(n)]
+    rows = [r.copy() for r in g]
+    sent, recv = oracle.single_reducer_avg(rows)
+    for i in range(p):
+        want = X.div(_fold([r[i] for r in g], 0), n)
+        for r in rows:
+            assert Fraction(float(r[i])) == want
+    # the reducer receives and sends (N-1)P; every other worker P each way
+    assert recv[0] == sent[0] == (n - 1) * p
+    assert all(sent[m] == recv[m] == p for m in range(1, n))
+
+
+def test_single_reducer_cost_figures_of_the_pages():
+    f = _kv("gibiansky_cost_figures.txt")
+    p = 1000
+    for gpus, key in ((2, "single_reducer_extra_s_2gpu"), (10, "single_reducer_extra_s_10gpu")):
+        rows = [np.zeros(p, np.float32) for _ in range(gpus)]
+        sent, recv = oracle.single_reducer_avg(rows)
+        # the reducer's link carries its received elements: scale to 300M fp32
+        gb = recv[0] / p * f["params"] * f["bytes_per_param"] / 1e9
+        assert abs(gb / f["single_reducer_link_gbps"] - f[key]) < 1e-6
+
+
+def test_single_reducer_bf16_small_integers():
+    rng = np.random.default_rng(41)
+    n, p = 5, 17
+    vals, rows = _bf16_rows_from_ints(rng, n, p, 256)
+    oracle.single_reducer_avg(rows)
+    for i in range(p):
+        s = sum(int(v[i]) for v in vals)
+        assert X.bf16_value(rows[2][i]) == X.rn_bf16(X.rn_f32(Fraction(s, n)))
