@@ -20,7 +20,7 @@ __all__ = [
     "ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_staged_workspace_bytes",
     "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
     "RA_STAGED_STATIC_MAX_P", "RA_HOST_AUTO", "RA_HOST_DIRECT", "RA_HOST_STAGED", "ra_reduce_scatter_avg",
-    "ra_all_gather", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
+    "ra_all_gather", "ra_allreduce_avg_bf16_wire", "ra_allreduce_avg_single_reducer", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
 ]
 
 RA_F32 = 0
@@ -80,6 +80,8 @@ def load():
     lib.ra_allreduce_avg_staged_static.argtypes = [pvp, i32, i64, i32, ctypes.POINTER(_Traffic), vp]
     lib.ra_reduce_scatter_avg.argtypes = [pvp, i32, i64, i32, pvp, vp]
     lib.ra_all_gather.argtypes = [pvp, i32, i64, i32, pvp, vp]
+    lib.ra_allreduce_avg_bf16_wire.argtypes = [pvp, i32, i64, vp]
+    lib.ra_allreduce_avg_single_reducer.argtypes = [pvp, i32, i64, i32, ctypes.POINTER(_Traffic), vp]
     lib.ra_chunk_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.ra_chunk_range.restype = None
     lib.ra_status_str.argtypes = [i32]
@@ -87,7 +89,8 @@ def load():
     lib.ra_last_cuda_error.argtypes = []
     for nm in ("ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_bucket_plan",
                "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
-               "ra_reduce_scatter_avg", "ra_all_gather", "ra_last_cuda_error"):
+               "ra_reduce_scatter_avg", "ra_all_gather", "ra_allreduce_avg_bf16_wire",
+               "ra_allreduce_avg_single_reducer", "ra_last_cuda_error"):
         getattr(lib, nm).restype = i32
     _lib = lib
     return lib
@@ -276,6 +279,24 @@ def ra_all_gather(tensors, shards=None, stream=None) -> None:
     arr, n, p, dt, dev = _rows(tensors)
     sh = _shards(shards, tensors, n, p)
     _check(load().ra_all_gather(arr, n, p, dt, sh, _stream(stream, dev)), "ra_all_gather")
+
+
+def ra_allreduce_avg_bf16_wire(tensors, stream=None) -> None:
+    """bf16 all-reduce with every partial sum rounded to bf16 (a bf16 ring)."""
+    arr, n, p, dt, dev = _rows(tensors)
+    if dt != RA_BF16:
+        raise TypeError("ra_allreduce_avg_bf16_wire takes bfloat16 tensors")
+    _check(load().ra_allreduce_avg_bf16_wire(arr, n, p, _stream(stream, dev)), "ra_allreduce_avg_bf16_wire")
+
+
+def ra_allreduce_avg_single_reducer(tensors, stream=None):
+    """Mean by the single-reducer scheme (worker 0 sums in worker order);
+    returns that scheme's [(sent, received)] per worker."""
+    arr, n, p, dt, dev = _rows(tensors)
+    traffic = (_Traffic * n)()
+    _check(load().ra_allreduce_avg_single_reducer(arr, n, p, dt, traffic, _stream(stream, dev)),
+           "ra_allreduce_avg_single_reducer")
+    return [(traffic[k].sent, traffic[k].received) for k in range(n)]
 
 
 def ra_chunk_range(p: int, n: int, c: int):

@@ -74,13 +74,13 @@ void ring_segments(int64_t off, int64_t count, int n, std::vector<Seg> *out) {
 }
 
 ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, const Seg *segs, int nseg, bool vector,
-                    int mis, cudaStream_t s, void *const *aux = nullptr) {
+                    int mis, cudaStream_t s, void *const *aux = nullptr, bool bf16_wire = false) {
     FusedLaunch L;
     for (int k = 0; k < n; ++k) {
         L.rows[k] = bufs[k];
         L.aux[k] = aux ? aux[k] : nullptr;
     }
-    L.out = aux ? 2 : (w ? 1 : 0);
+    L.out = bf16_wire ? 3 : (aux ? 2 : (w ? 1 : 0));
     L.n = n;
     L.dtype = dtype;
     L.w = w;
@@ -444,6 +444,35 @@ ra_status ra_all_gather(void *const *bufs, int n, int64_t p, int dtype, void *co
     L.nseg = (int)segs.size();
     cudaError_t e = launch_all_gather(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RA_OK : cuda_fail(e);
+}
+
+ra_status ra_allreduce_avg_bf16_wire(void *const *bufs, int n, int64_t p, void *stream) {
+    ra_status st = check_rows(bufs, n, p, RA_BF16);
+    if (st != RA_OK || n == 1 || p == 0) return st;
+    std::vector<Seg> segs;
+    ring_segments(0, p, n, &segs);
+    int mis = 0;
+    const bool vector = common_misalignment(bufs, n, RA_BF16, &mis);
+    return run_fused(bufs, n, RA_BF16, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
+                     static_cast<cudaStream_t>(stream), nullptr, true);
+}
+
+ra_status ra_allreduce_avg_single_reducer(void *const *bufs, int n, int64_t p, int dtype, ra_traffic *per_worker,
+                                          void *stream) {
+    ra_status st = check_rows(bufs, n, p, dtype);
+    if (st != RA_OK) return st;
+    // Gibiansky, "The Communication Problem": the reducer (worker 0) receives
+    // every other worker's array and sends the mean back to each of them
+    if (per_worker) {
+        for (int m = 0; m < n; ++m) per_worker[m].sent = per_worker[m].received = m == 0 ? (int64_t)(n - 1) * p : p;
+    }
+    if (n == 1 || p == 0) return RA_OK;
+    // one segment: every element's sum starts at worker 0 and takes the
+    // workers in order
+    const Seg seg{0, p, 0, 0, 0};
+    int mis = 0;
+    const bool vector = common_misalignment(bufs, n, dtype, &mis);
+    return run_fused(bufs, n, dtype, nullptr, 0.f, &seg, 1, vector, mis, static_cast<cudaStream_t>(stream));
 }
 
 void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end) {

@@ -39,6 +39,14 @@ template <class E, int NT>
 static cudaError_t fused_launch_nt(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     const bool big = L.nseg > kSegSmall;
     if (L.out != kOutAll && big) return cudaErrorInvalidValue;  // SGD / reduce-scatter use n segments
+    if (L.out == kOutAllWire) {
+        if constexpr (sizeof(typename E::T) == 2) {
+            if (L.vector) return fused_launch_one<E, NT, kOutAllWire, true, kSegSmall>(L, ntiles, s);
+            return fused_launch_one<E, 0, kOutAllWire, false, kSegSmall>(L, ntiles, s);
+        } else {
+            return cudaErrorInvalidValue;  // bf16 arrays only
+        }
+    }
     if (L.vector) {
         if (L.out == kOutAllSgd) return fused_launch_one<E, NT, kOutAllSgd, true, kSegSmall>(L, ntiles, s);
         if (L.out == kOutOne) return fused_launch_one<E, NT, kOutOne, true, kSegSmall>(L, ntiles, s);

@@ -60,7 +60,7 @@ enum StagedOp { kOpScatter = 0, kOpDivide = 1, kOpGather = 2 };
 struct FusedLaunch {
     void *rows[RA_MAX_N];
     void *aux[RA_MAX_N];  // reduce-scatter: destination base per chunk
-    int out;              // 0: all workers, 1: all workers + SGD, 2: one destination per chunk
+    int out;              // 0: all workers, 1: + SGD, 2: one destination per chunk, 3: bf16 partials
     int n;
     int dtype;
     float *w;  // SGD weights

@@ -140,7 +140,12 @@ __device__ __forceinline__ int ring_idx(int c, int k, int n) {
 // Where the fused kernel puts the mean: every worker's array (all-reduce),
 // the same plus the SGD step, or one destination per chunk (reduce-scatter:
 // the worker that owns the chunk, or a separate shard buffer).
-enum FusedOut { kOutAll = 0, kOutAllSgd = 1, kOutOne = 2 };
+// kOutAllWire: the all-reduce of bf16 arrays with every partial sum rounded
+// to bf16, as a ring that keeps its arrays in bf16 would store them.
+enum FusedOut { kOutAll = 0, kOutAllSgd = 1, kOutOne = 2, kOutAllWire = 3 };
+
+// binary32 value of the nearest bf16 (ties to even)
+__device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_f32(f32_to_bf16_bits(x)); }
 
 template <int MAXSEG>
 struct FusedParams {
@@ -177,7 +182,10 @@ template <class E, int NT, int OUT, int MAXSEG>
 __device__ __forceinline__ void fused_scalar(const FusedParams<MAXSEG> &p, int c, int64_t i) {
     const int n = NT > 0 ? NT : p.n;
     float acc = load_scalar<E>(p.rows[c], i);
-    for (int k = 1; k < n; ++k) acc = __fadd_rn(load_scalar<E>(p.rows[ring_idx(c, k, n)], i), acc);
+    for (int k = 1; k < n; ++k) {
+        acc = __fadd_rn(load_scalar<E>(p.rows[ring_idx(c, k, n)], i), acc);
+        if constexpr (OUT == kOutAllWire) acc = round_bf16(acc);
+    }
     const float avg = div_n<NT>(acc, n);
     if constexpr (OUT == kOutOne) {
         store_scalar_all<E>(&p.aux[c], 1, i, avg);
@@ -250,7 +258,10 @@ __device__ __forceinline__ void fused_vectors(const FusedParams<MAXSEG> &p, int 
                 for (int k = 1; k < NT; ++k) {
                     unpack<E>(x[j][k], t);
 #pragma unroll
-                    for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(t[e], acc[e]);
+                    for (int e = 0; e < V; ++e) {
+                        acc[e] = __fadd_rn(t[e], acc[e]);
+                        if constexpr (OUT == kOutAllWire) acc[e] = round_bf16(acc[e]);
+                    }
                 }
                 float avg[V];
 #pragma unroll
@@ -278,7 +289,10 @@ __device__ __forceinline__ void fused_vectors(const FusedParams<MAXSEG> &p, int 
                     } else {
                         unpack<E>(x[g], t);
 #pragma unroll
-                        for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(t[e], acc[e]);
+                        for (int e = 0; e < V; ++e) {
+                            acc[e] = __fadd_rn(t[e], acc[e]);
+                            if constexpr (OUT == kOutAllWire) acc[e] = round_bf16(acc[e]);
+                        }
                     }
                 }
             }

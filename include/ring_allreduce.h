@@ -247,6 +247,33 @@ ra_status ra_reduce_scatter_avg(void *const *bufs, int n, int64_t p, int dtype, 
  */
 ra_status ra_all_gather(void *const *bufs, int n, int64_t p, int dtype, void *const *shards, void *stream);
 
+/*
+ * ra_allreduce_avg_bf16_wire -- the ring over bf16 arrays as a ring that
+ * keeps every array in bf16 computes it: each receiver adds its own value
+ * and the received partial in binary32 and stores the sum back in bf16
+ * (nearest even), so every partial sum is rounded; the owner divides its
+ * bf16 sum by N in binary32 and rounds the mean to bf16 (Gibiansky,
+ * "Scatter-Reduce" with bf16 buffers).  Less accurate than ra_allreduce_avg
+ * with RA_BF16, whose partials stay binary32; offered to reproduce such
+ * rings bit for bit.  One fused pass, same traffic as ra_allreduce_avg.
+ */
+ra_status ra_allreduce_avg_bf16_wire(void *const *bufs, int n, int64_t p, void *stream);
+
+/*
+ * ra_allreduce_avg_single_reducer -- the averaging scheme the ring replaces
+ * (Gibiansky, "The Communication Problem"): every worker sends its gradient
+ * to one reducer, worker 0, which adds them in worker order
+ * ((g_0 + g_1) + g_2) + ... + g_{N-1} in binary32, divides by N, and sends
+ * the mean back to every worker.  Computed in one fused pass here; the
+ * result differs from the ring's only in summation order.
+ *   per_worker  optional HOST array of n ra_traffic entries: the elements
+ *               each worker sends and receives in that scheme -- (N-1)*P
+ *               each way for the reducer, P each way for every other worker
+ *               (the reducer's load grows with N, the ring's does not)
+ */
+ra_status ra_allreduce_avg_single_reducer(void *const *bufs, int n, int64_t p, int dtype, ra_traffic *per_worker,
+                                          void *stream);
+
 /* ra_chunk_range -- [begin, end) of chunk c of a p-element array split for
  * n workers (the first p mod n chunks hold one extra element). */
 void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end);
