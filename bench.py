@@ -365,6 +365,70 @@ def run_ours(args):
     return 0
 
 
+def run_overlap(args):
+    """Overlap of the bucketed all-reduce with a synthetic backward pass
+    (Gibiansky, "Applying the Allreduce to Deep Learning").  The backward of
+    the 24-layer Transformer is stood in for by bf16 tensor-core GEMMs, layer
+    by layer from the output side, sized at 4 * tokens * params FLOPs per
+    layer (weight and input gradients); as each layer's GEMMs are queued its
+    tensors are marked ready on the reducer, whose bucket all-reduces run on
+    their own stream.  Prints one JSON line with the four timings."""
+    import torch
+    from gradient_ring_all_gb300 import build
+    build.build()
+    import gradient_ring_all_gb300 as ra
+    import synth
+    wl = synth.WORKLOADS["transformer24_buckets_n4_f32"]
+    n, p, numel = wl.n, wl.p, list(wl.tensors)
+    rows = [torch.zeros(p, dtype=torch.float32, device="cuda") for _ in range(n)]
+    tokens = args.tokens
+    # GEMM unit: [tokens x 2048] @ [2048 x 8192] bf16
+    a = torch.randn(tokens, 2048, device="cuda", dtype=torch.bfloat16)
+    b = torch.randn(2048, 8192, device="cuda", dtype=torch.bfloat16)
+    unit_flops = 2.0 * tokens * 2048 * 8192
+    # layers: embed, 24 x 16 tensors, softmax -> groups of tensor indices
+    groups = [[0]] + [list(range(1 + 16 * l, 17 + 16 * l)) for l in range(24)] + [[len(numel) - 1]]
+    reps = [max(1, round(4.0 * tokens * sum(numel[t] for t in g) / unit_flops)) for g in groups]
+    stream = torch.cuda.current_stream()
+    red = ra.Reducer(rows, numel, wl.bucket_cap_bytes)
+
+    def backward(mark):
+        for g, r in zip(reversed(groups), reversed(reps)):
+            for _ in range(r):
+                torch.mm(a, b)
+            if mark:
+                for t in reversed(g):
+                    red.mark_ready(t, stream)
+
+    def t_of(fn, steps):
+        fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    plan = red.buckets()
+    steps = max(3, min(args.steps, 10))
+    t_bwd = t_of(lambda: backward(False), steps)
+    t_ar = t_of(lambda: ra.ra_allreduce_avg_buckets(rows, plan, stream), steps)
+    t_seq = t_of(lambda: (backward(False), ra.ra_allreduce_avg_buckets(rows, plan, stream)), steps)
+    t_ovl = t_of(lambda: (backward(True), red.finish(stream)), steps)
+    red.close()
+    line = {"experiment": "overlap of the bucketed all-reduce with a synthetic backward",
+            "workload": "transformer24_buckets_n4_f32", "buckets": len(plan), "tokens": tokens,
+            "backward_tflop": sum(reps) * unit_flops / 1e12,
+            "ms": {"backward": t_bwd, "allreduce": t_ar, "sequential": t_seq, "overlapped": t_ovl},
+            "exposed_allreduce_ms": t_ovl - t_bwd,
+            "hidden_fraction": (t_seq - t_ovl) / t_ar if t_ar > 0 else None}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -375,11 +439,16 @@ def main(argv=None):
                     help="profiling only: elements per worker instead of the workload's 300M")
     ap.add_argument("--legs", choices=["all", "device"], default="all",
                     help="profiling only: 'device' skips the end-to-end and CPU legs")
+    ap.add_argument("--overlap", action="store_true",
+                    help="experiment: bucketed all-reduce overlapped with a synthetic backward")
+    ap.add_argument("--tokens", type=int, default=8192, help="--overlap: tokens per backward step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.overlap:
+        return run_overlap(args)
     return run_ours(args)
 
 

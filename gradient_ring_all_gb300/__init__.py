@@ -20,7 +20,7 @@ __all__ = [
     "ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_staged_workspace_bytes",
     "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
     "RA_STAGED_STATIC_MAX_P", "RA_HOST_AUTO", "RA_HOST_DIRECT", "RA_HOST_STAGED", "ra_reduce_scatter_avg",
-    "ra_all_gather", "ra_allreduce_avg_bf16_wire", "ra_allreduce_avg_single_reducer", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
+    "ra_all_gather", "ra_allreduce_avg_bf16_wire", "ra_allreduce_avg_single_reducer", "Reducer", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
 ]
 
 RA_F32 = 0
@@ -82,6 +82,12 @@ def load():
     lib.ra_all_gather.argtypes = [pvp, i32, i64, i32, pvp, vp]
     lib.ra_allreduce_avg_bf16_wire.argtypes = [pvp, i32, i64, vp]
     lib.ra_allreduce_avg_single_reducer.argtypes = [pvp, i32, i64, i32, ctypes.POINTER(_Traffic), vp]
+    lib.ra_reducer_create.argtypes = [pvp, i32, i32, ctypes.POINTER(ctypes.c_int64), i32, i64,
+                                      ctypes.POINTER(ctypes.c_void_p)]
+    lib.ra_reducer_buckets.argtypes = [vp, ctypes.POINTER(_Bucket), i32, ctypes.POINTER(i32)]
+    lib.ra_reducer_mark_ready.argtypes = [vp, i32, vp]
+    lib.ra_reducer_finish.argtypes = [vp, vp]
+    lib.ra_reducer_destroy.argtypes = [vp]
     lib.ra_chunk_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.ra_chunk_range.restype = None
     lib.ra_status_str.argtypes = [i32]
@@ -90,7 +96,8 @@ def load():
     for nm in ("ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_bucket_plan",
                "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
                "ra_reduce_scatter_avg", "ra_all_gather", "ra_allreduce_avg_bf16_wire",
-               "ra_allreduce_avg_single_reducer", "ra_last_cuda_error"):
+               "ra_allreduce_avg_single_reducer", "ra_reducer_create", "ra_reducer_buckets",
+               "ra_reducer_mark_ready", "ra_reducer_finish", "ra_reducer_destroy", "ra_last_cuda_error"):
         getattr(lib, nm).restype = i32
     _lib = lib
     return lib
@@ -297,6 +304,53 @@ def ra_allreduce_avg_single_reducer(tensors, stream=None):
     _check(load().ra_allreduce_avg_single_reducer(arr, n, p, dt, traffic, _stream(stream, dev)),
            "ra_allreduce_avg_single_reducer")
     return [(traffic[k].sent, traffic[k].received) for k in range(n)]
+
+
+class Reducer:
+    """ra_reducer: buckets of layer tensors all-reduced as their gradients
+    become ready (output layer first), on a stream of the reducer's own.
+
+    flat_tensors: one contiguous CUDA tensor per worker holding the layer
+    gradients back to back in forward order; numel: the layer sizes."""
+
+    def __init__(self, flat_tensors, numel, cap_bytes: int):
+        flat_tensors = list(flat_tensors)
+        arr, n, p, dt, dev = _rows(flat_tensors)
+        numel = [int(x) for x in numel]
+        if sum(numel) != p:
+            raise ValueError("the layer sizes must add up to the flat length")
+        self._keep = flat_tensors
+        self.device = dev
+        cnt = (ctypes.c_int64 * max(1, len(numel)))(*numel)
+        h = ctypes.c_void_p()
+        _check(load().ra_reducer_create(arr, n, dt, cnt, len(numel), int(cap_bytes), ctypes.byref(h)),
+               "ra_reducer_create")
+        self._h = h
+        self.ntensors = len(numel)
+
+    def buckets(self):
+        out = (_Bucket * (self.ntensors + 1))()
+        nb = ctypes.c_int(0)
+        _check(load().ra_reducer_buckets(self._h, out, self.ntensors + 1, ctypes.byref(nb)), "ra_reducer_buckets")
+        return [(out[k].offset, out[k].count) for k in range(nb.value)]
+
+    def mark_ready(self, tensor: int, stream=None) -> None:
+        _check(load().ra_reducer_mark_ready(self._h, int(tensor), _stream(stream, self.device)),
+               "ra_reducer_mark_ready")
+
+    def finish(self, stream=None) -> None:
+        _check(load().ra_reducer_finish(self._h, _stream(stream, self.device)), "ra_reducer_finish")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _check(load().ra_reducer_destroy(self._h), "ra_reducer_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def ra_chunk_range(p: int, n: int, c: int):

@@ -37,21 +37,6 @@ bool ranges_disjoint(std::vector<std::pair<uintptr_t, uintptr_t>> r) {
     return true;
 }
 
-// Checks shared by every call that reads `bufs` of p elements.
-ra_status check_rows(void *const *bufs, int n, int64_t p, int dtype) {
-    if (n < 1 || n > RA_MAX_N || p < 0 || elem_size(dtype) == 0 || bufs == nullptr) return RA_ERR_INVALID_ARG;
-    const int esz = elem_size(dtype);
-    if (p > INT64_MAX / 16) return RA_ERR_INVALID_ARG;
-    if (p == 0) return RA_OK;
-    std::vector<std::pair<uintptr_t, uintptr_t>> r;
-    for (int k = 0; k < n; ++k) {
-        const uintptr_t a = reinterpret_cast<uintptr_t>(bufs[k]);
-        if (a == 0 || a % esz != 0) return RA_ERR_INVALID_ARG;
-        r.emplace_back(a, a + (uintptr_t)p * esz);
-    }
-    return ranges_disjoint(std::move(r)) ? RA_OK : RA_ERR_OVERLAP;
-}
-
 // 16-byte vector path: all rows (and the extra pointer, if any, holding
 // binary32 elements indexed like the rows) sit the same number of elements
 // past a 16-byte boundary.
@@ -133,6 +118,21 @@ ra_status shard_bases(void *const *bufs, int n, int64_t p, int dtype, void *cons
 }
 
 }  // namespace
+
+// Checks shared by every call that reads `bufs` of p elements.
+ra_status check_rows(void *const *bufs, int n, int64_t p, int dtype) {
+    if (n < 1 || n > RA_MAX_N || p < 0 || elem_size(dtype) == 0 || bufs == nullptr) return RA_ERR_INVALID_ARG;
+    const int esz = elem_size(dtype);
+    if (p > INT64_MAX / 16) return RA_ERR_INVALID_ARG;
+    if (p == 0) return RA_OK;
+    std::vector<std::pair<uintptr_t, uintptr_t>> r;
+    for (int k = 0; k < n; ++k) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(bufs[k]);
+        if (a == 0 || a % esz != 0) return RA_ERR_INVALID_ARG;
+        r.emplace_back(a, a + (uintptr_t)p * esz);
+    }
+    return ranges_disjoint(std::move(r)) ? RA_OK : RA_ERR_OVERLAP;
+}
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 

@@ -112,4 +112,7 @@ int fused_compile_time_n(int n);  // the specialised worker count used for n (0 
 // set the value ra_last_cuda_error() reports on this thread
 void record_cuda_error(cudaError_t e);
 
+// argument checks shared by the calls that take n worker arrays of p elements
+ra_status check_rows(void *const *bufs, int n, int64_t p, int dtype);
+
 }  // namespace ra

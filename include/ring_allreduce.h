@@ -274,6 +274,42 @@ ra_status ra_allreduce_avg_bf16_wire(void *const *bufs, int n, int64_t p, void *
 ra_status ra_allreduce_avg_single_reducer(void *const *bufs, int n, int64_t p, int dtype, ra_traffic *per_worker,
                                           void *stream);
 
+/*
+ * ra_reducer -- per-bucket all-reduce overlapped with the backward pass
+ * (Gibiansky, "Applying the Allreduce to Deep Learning": backpropagation
+ * yields the output layer's gradients first and the all-reduce can run on a
+ * subset of the parameters, so communication starts while earlier layers
+ * are still computing).
+ *
+ * The reducer holds the ra_bucket_plan of a model's layer tensors (forward
+ * order, packed back to back in every worker's flat gradient array) and a
+ * stream of its own.  Each step the training loop calls
+ * ra_reducer_mark_ready(tensor, stream) once per tensor, when the work that
+ * completes that tensor's gradient (on every worker) has been queued on
+ * `stream`; as soon as all tensors of a bucket are marked, the bucket's ring
+ * all-reduce (the same bits as ra_allreduce_avg_buckets) is queued on the
+ * reducer's stream behind an event recorded on `stream`.
+ * ra_reducer_finish(stream) queues the buckets whose tensors were not all
+ * marked, makes `stream` wait for every bucket, and resets the marks for
+ * the next step.  A reducer belongs to the device current at creation and
+ * to one host thread at a time; it allocates host memory, one stream and
+ * nb + 1 events, but no device memory.
+ *   ra_reducer_create   bufs: n device pointers, each holding sum(numel)
+ *                       elements of dtype; numel: host array of ntensors
+ *                       element counts; cap_bytes: bucket size (> 0)
+ *   ra_reducer_buckets  copies the plan (closing order) into out[max_out]
+ *   ra_reducer_destroy  waits for the reducer's stream, then frees it
+ * RA_ERR_INVALID_ARG for a tensor marked twice in one step or a call from
+ * another device.
+ */
+typedef struct ra_reducer ra_reducer;
+ra_status ra_reducer_create(void *const *bufs, int n, int dtype, const int64_t *numel, int ntensors,
+                            int64_t cap_bytes, ra_reducer **out);
+ra_status ra_reducer_buckets(const ra_reducer *r, ra_bucket *out, int max_out, int *n_out);
+ra_status ra_reducer_mark_ready(ra_reducer *r, int tensor, void *stream);
+ra_status ra_reducer_finish(ra_reducer *r, void *stream);
+ra_status ra_reducer_destroy(ra_reducer *r);
+
 /* ra_chunk_range -- [begin, end) of chunk c of a p-element array split for
  * n workers (the first p mod n chunks hold one extra element). */
 void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end);
