@@ -365,6 +365,90 @@ def run_ours(args):
     return 0
 
 
+CALLS = ("allreduce", "staged", "sgd", "buckets", "reduce_scatter", "all_gather", "single_reducer", "bf16_wire",
+         "host")
+
+
+def call_bytes(call: str, n: int, p: int, esz: int) -> int:
+    """Algorithmic bytes one call moves: every byte its design must read or
+    write once (the staged ring's own schedule for `staged`)."""
+    if call in ("allreduce", "buckets", "single_reducer", "bf16_wire", "host"):
+        return 2 * n * p * esz
+    if call == "sgd":
+        return 2 * n * p * esz + 2 * p * 4
+    if call == "reduce_scatter":
+        return (n + 1) * p * esz
+    if call == "all_gather":
+        return n * p * esz
+    if call == "staged":
+        if esz == 4:  # in place: 3P per scatter step, 2P divide, 2P per gather step
+            return (5 * (n - 1) + 2) * p * 4
+        # bf16: binary32 partials -- 2+2+4 (first step), 2+4+4 (others), 4+2 divide, 2+2 per gather
+        return (8 + 10 * (n - 2) + 6 + 4 * (n - 1)) * p
+    raise ValueError(call)
+
+
+def run_profile_call(args):
+    """Device-only timing of one entry point on one workload (the launch
+    configuration profiled under ncu); inputs from a seeded torch generator
+    on the device, since only the traffic matters here."""
+    import torch
+    from gradient_ring_all_gb300 import build
+    build.build()
+    import gradient_ring_all_gb300 as ra
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    n, p = wl.n, (args.elements or wl.p)
+    bf16 = wl.dtype == "bf16"
+    esz = 2 if bf16 else 4
+    g = torch.Generator(device="cuda")
+    g.manual_seed(wl.seed)
+    rows = []
+    for _ in range(n):
+        r = torch.empty(p, dtype=torch.bfloat16 if bf16 else torch.float32, device="cuda")
+        tmp = torch.randn(p, generator=g, device="cuda") * wl.scale
+        r.copy_(tmp)
+        del tmp
+        rows.append(r)
+    stream = torch.cuda.current_stream()
+    c = args.call
+    if c == "allreduce":
+        step = lambda: ra.ra_allreduce_avg(rows, stream)
+    elif c == "staged":
+        ws = torch.empty(max(1, ra.ra_staged_workspace_bytes(n, p, 1 if bf16 else 0)), dtype=torch.uint8,
+                         device="cuda")
+        step = lambda: ra.ra_allreduce_avg_staged(rows, ws, stream)
+    elif c == "sgd":
+        w = torch.randn(p, generator=g, device="cuda")
+        step = lambda: ra.ra_allreduce_sgd(rows, w, wl.sgd_lr or 0.1, stream)
+    elif c == "buckets":
+        plan = ra.ra_bucket_plan(wl.tensors, esz, wl.bucket_cap_bytes or 25 * 1024 * 1024)
+        step = lambda: ra.ra_allreduce_avg_buckets(rows, plan, stream)
+    elif c == "reduce_scatter":
+        step = lambda: ra.ra_reduce_scatter_avg(rows, None, stream)
+    elif c == "all_gather":
+        step = lambda: ra.ra_all_gather(rows, None, stream)
+    elif c == "single_reducer":
+        step = lambda: ra.ra_allreduce_avg_single_reducer(rows, stream)
+    elif c == "bf16_wire":
+        step = lambda: ra.ra_allreduce_avg_bf16_wire(rows, stream)
+    else:  # host: the rows live in pinned host memory, the kernel works on them directly
+        hrows = [torch.empty(p, dtype=rows[0].dtype).pin_memory() for _ in range(n)]
+        for h, r in zip(hrows, rows):
+            h.copy_(r)
+        del rows
+        step = lambda: ra.ra_allreduce_avg_host(hrows, None, ra.RA_HOST_DIRECT, stream)
+    for _ in range(args.warmup):
+        step()
+    _, ms = timed_region(lambda k: step(), args.steps, None, _CudaEventTimer(stream))
+    ms /= args.steps
+    nbytes = call_bytes(c, n, p, esz)
+    print(json.dumps({"profile_run": True, "workload": args.workload, "call": c, "workers": n,
+                      "elements_per_worker": p, "ms_per_step": ms, "algorithmic_bytes": nbytes,
+                      "gbs": nbytes / (ms / 1e3) / 1e9}), flush=True)
+    return 0
+
+
 def run_overlap(args):
     """Overlap of the bucketed all-reduce with a synthetic backward pass
     (Gibiansky, "Applying the Allreduce to Deep Learning").  The backward of
@@ -439,6 +523,10 @@ def main(argv=None):
                     help="profiling only: elements per worker instead of the workload's 300M")
     ap.add_argument("--legs", choices=["all", "device"], default="all",
                     help="profiling only: 'device' skips the end-to-end and CPU legs")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="profiling only (with --call): the synthetic workload to run")
+    ap.add_argument("--call", choices=CALLS, default=None,
+                    help="profiling only: time one entry point on --workload, device loop only")
     ap.add_argument("--overlap", action="store_true",
                     help="experiment: bucketed all-reduce overlapped with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=8192, help="--overlap: tokens per backward step")
@@ -449,6 +537,8 @@ def main(argv=None):
         return run_reference(args)
     if args.overlap:
         return run_overlap(args)
+    if args.call:
+        return run_profile_call(args)
     return run_ours(args)
 
 
