@@ -341,7 +341,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "kernel": "fused_allreduce_kernel<F32, N=8>", "avg_launch_ms": avg_kernel_ms,
+                     "kernel": "fused_tma_kernel<F32, N=8, kOutAll>", "avg_launch_ms": avg_kernel_ms,
                      "traffic": _traffic_from_profile("fused_f32_n8_speech300m")},
         "e2e": {"value": aggregate_gbs(nbytes, ws, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": n * p * 4, "d2h_bytes_per_step": n * p * 4,

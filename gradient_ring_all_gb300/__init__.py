@@ -20,7 +20,7 @@ __all__ = [
     "ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_staged_workspace_bytes",
     "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
     "RA_STAGED_STATIC_MAX_P", "RA_HOST_AUTO", "RA_HOST_DIRECT", "RA_HOST_STAGED", "ra_reduce_scatter_avg",
-    "ra_all_gather", "ra_allreduce_avg_bf16_wire", "ra_allreduce_avg_single_reducer", "Reducer", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
+    "ra_all_gather", "ra_allreduce_avg_bf16_wire", "ra_allreduce_avg_single_reducer", "Reducer", "ra_check_device_errors", "ra_selftest_wait_timeout", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
 ]
 
 RA_F32 = 0
@@ -88,6 +88,8 @@ def load():
     lib.ra_reducer_mark_ready.argtypes = [vp, i32, vp]
     lib.ra_reducer_finish.argtypes = [vp, vp]
     lib.ra_reducer_destroy.argtypes = [vp]
+    lib.ra_check_device_errors.argtypes = []
+    lib.ra_selftest_wait_timeout.argtypes = [i32, vp]
     lib.ra_chunk_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.ra_chunk_range.restype = None
     lib.ra_status_str.argtypes = [i32]
@@ -97,7 +99,8 @@ def load():
                "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
                "ra_reduce_scatter_avg", "ra_all_gather", "ra_allreduce_avg_bf16_wire",
                "ra_allreduce_avg_single_reducer", "ra_reducer_create", "ra_reducer_buckets",
-               "ra_reducer_mark_ready", "ra_reducer_finish", "ra_reducer_destroy", "ra_last_cuda_error"):
+               "ra_reducer_mark_ready", "ra_reducer_finish", "ra_reducer_destroy", "ra_check_device_errors",
+               "ra_selftest_wait_timeout", "ra_last_cuda_error"):
         getattr(lib, nm).restype = i32
     _lib = lib
     return lib
@@ -351,6 +354,19 @@ class Reducer:
             self.close()
         except Exception:
             pass
+
+
+def ra_check_device_errors() -> int:
+    """Status of the kernels' bounded waits on the current device since the
+    last check: 0 (RA_OK) or 5 (RA_ERR_TIMEOUT); clears the record."""
+    return int(load().ra_check_device_errors())
+
+
+def ra_selftest_wait_timeout(timeout_us: int, stream=None) -> None:
+    """Queue a kernel whose bounded wait is made to expire (a timeout test)."""
+    import torch
+    _check(load().ra_selftest_wait_timeout(int(timeout_us), _stream(stream, torch.device("cuda", torch.cuda.current_device()))),
+           "ra_selftest_wait_timeout")
 
 
 def ra_chunk_range(p: int, n: int, c: int):

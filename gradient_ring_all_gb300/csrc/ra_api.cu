@@ -73,7 +73,9 @@ ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, con
     L.vector = vector;
     L.mis = mis;
     std::vector<Seg> tab(segs, segs + nseg);
-    const int64_t ntiles = fused_assign_tiles(tab.data(), nseg, n, dtype, vector, mis);
+    L.tile_bytes = fused_tile_bytes(n);
+    const int64_t ntiles = vector ? fused_tma_assign_tiles(tab.data(), nseg, dtype, mis, L.tile_bytes)
+                                  : fused_scalar_assign_tiles(tab.data(), nseg);
     L.seg = tab.data();
     L.nseg = nseg;
     if (ntiles == 0) return RA_OK;
@@ -136,29 +138,24 @@ ra_status check_rows(void *const *bufs, int n, int64_t p, int dtype) {
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
-int fused_compile_time_n(int n) {
-    switch (n) {
-        case 2: case 4: case 8: case 16: case 32: return n;
-        default: return 0;
-    }
-}
-
-int64_t fused_assign_tiles(Seg *seg, int nseg, int n, int dtype, bool vector, int mis) {
-    const int V = vec_elems(dtype);
-    const int64_t tv = fused_tile_vectors(fused_compile_time_n(n));
+int64_t fused_scalar_assign_tiles(Seg *seg, int nseg) {
     const int64_t ts = (int64_t)kThreadsPerBlock * kScalarPerThread;
     int64_t t = 0;
     for (int k = 0; k < nseg; ++k) {
         seg[k].tile0 = t;
-        int64_t tiles;
-        if (vector) {
-            int64_t ab, ae;
-            vector_interior(seg[k].begin, seg[k].end, mis, V, &ab, &ae);
-            tiles = std::max<int64_t>(1, ((ae - ab) / V + tv - 1) / tv);
-        } else {
-            tiles = std::max<int64_t>(1, (seg[k].end - seg[k].begin + ts - 1) / ts);
-        }
-        t += tiles;
+        t += std::max<int64_t>(1, (seg[k].end - seg[k].begin + ts - 1) / ts);
+    }
+    return t;
+}
+
+int64_t fused_tma_assign_tiles(Seg *seg, int nseg, int dtype, int mis, int tile_bytes) {
+    const int V = vec_elems(dtype), esz = elem_size(dtype);
+    int64_t t = 0;
+    for (int k = 0; k < nseg; ++k) {
+        seg[k].tile0 = t;
+        int64_t ab, ae;
+        vector_interior(seg[k].begin, seg[k].end, mis, V, &ab, &ae);
+        t += std::max<int64_t>(1, ((ae - ab) * esz + tile_bytes - 1) / tile_bytes);
     }
     return t;
 }
@@ -473,6 +470,20 @@ ra_status ra_allreduce_avg_single_reducer(void *const *bufs, int n, int64_t p, i
     int mis = 0;
     const bool vector = common_misalignment(bufs, n, dtype, &mis);
     return run_fused(bufs, n, dtype, nullptr, 0.f, &seg, 1, vector, mis, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ra_check_device_errors(void) {
+    unsigned int flags = 0;
+    cudaError_t e = collect_device_error_f32(&flags);
+    if (e == cudaSuccess) e = collect_device_error_bf16(&flags);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return flags ? RA_ERR_TIMEOUT : RA_OK;
+}
+
+ra_status ra_selftest_wait_timeout(int timeout_us, void *stream) {
+    if (timeout_us < 1 || timeout_us > 10000000) return RA_ERR_INVALID_ARG;
+    cudaError_t e = launch_wait_timeout_selftest((uint64_t)timeout_us * 1000ull, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RA_OK : cuda_fail(e);
 }
 
 void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end) {

@@ -9,8 +9,9 @@
 
 namespace ra {
 
-template <class E, int NT, int OUT, bool VEC, int MAXSEG>
-static cudaError_t fused_launch_one(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+// scalar path (rows that disagree modulo 16 bytes): element by element
+template <class E, int OUT, int MAXSEG>
+static cudaError_t fused_scalar_launch_one(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     FusedParams<MAXSEG> p;
     memset(&p, 0, sizeof(p));
     for (int k = 0; k < L.n; ++k) {
@@ -31,45 +32,114 @@ static cudaError_t fused_launch_one(const FusedLaunch &L, int64_t ntiles, cudaSt
     // 6.28 TB/s at N=8, P=300M f32).  The kernel's tile loop only matters
     // past 2^31-1 tiles.
     const int64_t grid = ntiles < kMaxGrid ? ntiles : kMaxGrid;
-    fused_allreduce_kernel<E, NT, OUT, VEC, MAXSEG><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    fused_scalar_kernel<E, OUT, MAXSEG><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <class E, int NT>
-static cudaError_t fused_launch_nt(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+template <class E>
+static cudaError_t fused_scalar_dispatch(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     const bool big = L.nseg > kSegSmall;
-    if (L.out != kOutAll && big) return cudaErrorInvalidValue;  // SGD / reduce-scatter use n segments
-    if (L.out == kOutAllWire) {
-        if constexpr (sizeof(typename E::T) == 2) {
-            if (L.vector) return fused_launch_one<E, NT, kOutAllWire, true, kSegSmall>(L, ntiles, s);
-            return fused_launch_one<E, 0, kOutAllWire, false, kSegSmall>(L, ntiles, s);
-        } else {
-            return cudaErrorInvalidValue;  // bf16 arrays only
-        }
+    if (L.out != kOutAll && big) return cudaErrorInvalidValue;
+    switch (L.out) {
+        case kOutAllSgd: return fused_scalar_launch_one<E, kOutAllSgd, kSegSmall>(L, ntiles, s);
+        case kOutOne: return fused_scalar_launch_one<E, kOutOne, kSegSmall>(L, ntiles, s);
+        case kOutAllWire:
+            if constexpr (sizeof(typename E::T) == 2)
+                return fused_scalar_launch_one<E, kOutAllWire, kSegSmall>(L, ntiles, s);
+            return cudaErrorInvalidValue;
+        default:
+            if (big) return fused_scalar_launch_one<E, kOutAll, kSegLarge>(L, ntiles, s);
+            return fused_scalar_launch_one<E, kOutAll, kSegSmall>(L, ntiles, s);
     }
-    if (L.vector) {
-        if (L.out == kOutAllSgd) return fused_launch_one<E, NT, kOutAllSgd, true, kSegSmall>(L, ntiles, s);
-        if (L.out == kOutOne) return fused_launch_one<E, NT, kOutOne, true, kSegSmall>(L, ntiles, s);
-        if (big) return fused_launch_one<E, NT, kOutAll, true, kSegLarge>(L, ntiles, s);
-        return fused_launch_one<E, NT, kOutAll, true, kSegSmall>(L, ntiles, s);
+}
+
+template <class E, int NT, int OUT, int MAXSEG>
+static cudaError_t fused_tma_launch_one(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+    auto kern = fused_tma_kernel<E, NT, OUT, MAXSEG>;
+    // large dynamic shared memory needs an opt-in per kernel and device
+    static unsigned long long opted_in = 0;  // bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !(__atomic_load_n(&opted_in, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&opted_in, 1ull << dev, __ATOMIC_ACQ_REL);
     }
-    // scalar path: generic worker count only
-    if (L.out == kOutAllSgd) return fused_launch_one<E, 0, kOutAllSgd, false, kSegSmall>(L, ntiles, s);
-    if (L.out == kOutOne) return fused_launch_one<E, 0, kOutOne, false, kSegSmall>(L, ntiles, s);
-    if (big) return fused_launch_one<E, 0, kOutAll, false, kSegLarge>(L, ntiles, s);
-    return fused_launch_one<E, 0, kOutAll, false, kSegSmall>(L, ntiles, s);
+    TmaFusedParams<MAXSEG> tp;
+    memset(&tp, 0, sizeof(tp));
+    FusedParams<MAXSEG> &p = tp.f;
+    for (int k = 0; k < L.n; ++k) {
+        p.rows[k] = L.rows[k];
+        p.aux[k] = L.aux[k];
+    }
+    p.w = L.w;
+    p.lr = L.lr;
+    p.n = L.n;
+    p.nseg = L.nseg;
+    p.mis = L.mis;
+    p.ntiles = ntiles;
+    for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
+    tp.tile_bytes = L.tile_bytes;
+    const int esz = (int)sizeof(typename E::T);
+    const size_t smem = (size_t)L.n * L.tile_bytes + L.tile_bytes + (OUT == kOutAllSgd ? L.tile_bytes / esz * 4 : 0) + 16;
+    if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;
+    // one tile per block (see fused_scalar_launch_one)
+    const int64_t grid = ntiles < kMaxGrid ? ntiles : kMaxGrid;
+    kern<<<(unsigned)grid, kThreadsPerBlock, smem, s>>>(tp);
+    return cudaGetLastError();
+}
+
+// vector path: the TMA kernel, the fold unrolled for the common worker counts
+template <class E, int NT>
+static cudaError_t fused_tma_dispatch_nt(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+    const bool big = L.nseg > kSegSmall;
+    if (L.out != kOutAll && big) return cudaErrorInvalidValue;
+    switch (L.out) {
+        case kOutAllSgd: return fused_tma_launch_one<E, NT, kOutAllSgd, kSegSmall>(L, ntiles, s);
+        case kOutOne: return fused_tma_launch_one<E, NT, kOutOne, kSegSmall>(L, ntiles, s);
+        case kOutAllWire:
+            if constexpr (sizeof(typename E::T) == 2)
+                return fused_tma_launch_one<E, NT, kOutAllWire, kSegSmall>(L, ntiles, s);
+            return cudaErrorInvalidValue;
+        default:
+            if (big) return fused_tma_launch_one<E, NT, kOutAll, kSegLarge>(L, ntiles, s);
+            return fused_tma_launch_one<E, NT, kOutAll, kSegSmall>(L, ntiles, s);
+    }
+}
+
+// Which worker counts get the unrolled fold was measured on GB300: it wins at
+// n = 4 (7.05 vs 6.92 TB/s), ties at 8, edges ahead for binary32 at 32, and
+// loses for bf16 at 16 (6.89 vs 7.05 TB/s), where the runtime loop is kept.
+template <class E>
+static cudaError_t fused_tma_dispatch(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+    constexpr bool wide = sizeof(typename E::T) == 4;
+    switch (L.n) {
+        case 2: return fused_tma_dispatch_nt<E, 2>(L, ntiles, s);
+        case 4: return fused_tma_dispatch_nt<E, 4>(L, ntiles, s);
+        case 8: return fused_tma_dispatch_nt<E, 8>(L, ntiles, s);
+        case 16:
+            if constexpr (wide) return fused_tma_dispatch_nt<E, 16>(L, ntiles, s);
+            return fused_tma_dispatch_nt<E, 0>(L, ntiles, s);
+        case 32:
+            if constexpr (wide) return fused_tma_dispatch_nt<E, 32>(L, ntiles, s);
+            return fused_tma_dispatch_nt<E, 0>(L, ntiles, s);
+        default: return fused_tma_dispatch_nt<E, 0>(L, ntiles, s);
+    }
+}
+
+template <class E>
+static cudaError_t collect_device_error(unsigned int *flags) {
+    unsigned int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_ra_device_error, sizeof(v));
+    if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_ra_device_error, &zero, sizeof(zero));
+    *flags |= v;
+    return e;
 }
 
 template <class E>
 static cudaError_t fused_launch_dtype(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
-    switch (L.vector ? fused_compile_time_n(L.n) : 0) {
-        case 2: return fused_launch_nt<E, 2>(L, ntiles, s);
-        case 4: return fused_launch_nt<E, 4>(L, ntiles, s);
-        case 8: return fused_launch_nt<E, 8>(L, ntiles, s);
-        case 16: return fused_launch_nt<E, 16>(L, ntiles, s);
-        case 32: return fused_launch_nt<E, 32>(L, ntiles, s);
-        default: return fused_launch_nt<E, 0>(L, ntiles, s);
-    }
+    return L.vector ? fused_tma_dispatch<E>(L, ntiles, s) : fused_scalar_dispatch<E>(L, ntiles, s);
 }
 
 }  // namespace ra

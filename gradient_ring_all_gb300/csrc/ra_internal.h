@@ -26,16 +26,6 @@ constexpr int64_t kMaxGrid = 0x7fffffff;  // largest gridDim.x
 constexpr int kScalarPerThread = 4;  // elements per thread per tile, scalar path
 constexpr int kStagedTileVec = 512;  // 16-byte vectors per tile, staged kernel
 
-// 16-byte vectors each thread keeps in flight per worker in the fused
-// kernel, by compile-time worker count (0 = any count)
-__host__ __device__ constexpr int fused_vec_per_thread(int nt) {
-    return nt == 0 ? 1 : (nt <= 4 ? 4 : (nt <= 8 ? 2 : 1));
-}
-
-__host__ __device__ constexpr int64_t fused_tile_vectors(int nt) {
-    return (int64_t)kThreadsPerBlock * fused_vec_per_thread(nt);
-}
-
 // The 16-byte-vector interior [ab, ae) of the element range [b, e) when the
 // rows' addresses are `mis` elements past a 16-byte boundary (V elements per
 // vector): ab is the first index >= b with (index + mis) % V == 0, ae the
@@ -69,11 +59,31 @@ struct FusedLaunch {
     int mis;
     const Seg *seg;  // host table, tile0 filled by the launcher
     int nseg;
+    int tile_bytes;  // vector path: bytes per row per tile
 };
 
-// fill seg[].tile0 and return the tile count for the fused kernel chosen
-// for (n, dtype, vector)
-int64_t fused_assign_tiles(Seg *seg, int nseg, int n, int dtype, bool vector, int mis);
+// Vector path of the fused kernel: bytes of each row one block stages in
+// shared memory -- n rows plus one output tile fit about three blocks per SM.
+#ifndef RA_TMA_STAGE_BYTES
+#define RA_TMA_STAGE_BYTES 65536
+#endif
+inline int fused_tile_bytes(int n) {
+    int b = 16384;
+    while (b > 2048 && (int64_t)b * n > RA_TMA_STAGE_BYTES) b >>= 1;
+    return b;
+}
+constexpr int kMaxDynamicSmem = 227 * 1024;
+
+int64_t fused_tma_assign_tiles(Seg *seg, int nseg, int dtype, int mis, int tile_bytes);
+
+// collect and clear the device error flags of the fused-kernel translation units
+cudaError_t collect_device_error_f32(unsigned int *flags);
+cudaError_t collect_device_error_bf16(unsigned int *flags);
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t s);
+
+// fill seg[].tile0 and return the tile count: fused scalar kernel, staged
+// kernel, fused TMA kernel
+int64_t fused_scalar_assign_tiles(Seg *seg, int nseg);
 int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis);
 
 cudaError_t launch_fused_f32(const FusedLaunch &L, int64_t ntiles, cudaStream_t s);
@@ -106,8 +116,6 @@ struct GatherLaunch {
     int64_t ntiles;
 };
 cudaError_t launch_all_gather(const GatherLaunch &L, cudaStream_t s);
-
-int fused_compile_time_n(int n);  // the specialised worker count used for n (0 = generic)
 
 // set the value ra_last_cuda_error() reports on this thread
 void record_cuda_error(cudaError_t e);

@@ -197,138 +197,199 @@ __device__ __forceinline__ void fused_scalar(const FusedParams<MAXSEG> &p, int c
 
 constexpr int kThreads = kThreadsPerBlock;
 
-// store one vector of means (and apply the SGD step to the matching weights)
-template <class E, int NT, int OUT, int MAXSEG>
-__device__ __forceinline__ void fused_emit(const FusedParams<MAXSEG> &p, int c, int n, int64_t i,
-                                           const float (&avg)[E::kVec]) {
-    constexpr int V = E::kVec;
-    constexpr int esz = (int)sizeof(typename E::T);
-    float held[V];
-    const uint4 out = pack<E>(avg, held);
-    if constexpr (OUT == kOutOne) {
-        st_vec(reinterpret_cast<char *>(p.aux[c]) + i * esz, out);
-    } else {
-        if constexpr (NT > 0) {
-#pragma unroll
-            for (int k = 0; k < NT; ++k) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, out);
-        } else {
-            for (int k = 0; k < n; ++k) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, out);
-        }
-        if constexpr (OUT == kOutAllSgd) {
-#pragma unroll
-            for (int e = 0; e < V; e += 4) {
-                float4 *wp = reinterpret_cast<float4 *>(p.w + i + e);
-                float4 wv = __ldcs(wp);
-                wv.x = __fsub_rn(wv.x, __fmul_rn(p.lr, held[e + 0]));
-                wv.y = __fsub_rn(wv.y, __fmul_rn(p.lr, held[e + 1]));
-                wv.z = __fsub_rn(wv.z, __fmul_rn(p.lr, held[e + 2]));
-                wv.w = __fsub_rn(wv.w, __fmul_rn(p.lr, held[e + 3]));
-                __stcs(wp, wv);
-            }
-        }
+// ---------------------------------------------------------------------------
+// TMA fused kernel (the vector path).  One block per tile; a tile is up to
+// tile_bytes of one segment's 16-byte-aligned interior in every row.  Thread
+// 0 starts n bulk copies (cp.async.bulk, global -> shared) that complete on
+// one mbarrier; every thread folds its 16-byte vectors over the n staged rows
+// in ring order straight from shared memory, writes the mean to a shared
+// output tile, and thread 0 stores that tile to every destination with bulk
+// copies (shared -> global).  The copy engine holds the bytes in flight, so
+// the fold needs no per-n register arrays and one kernel serves every n.
+
+// Device-side error flag, one per translation unit (bit 0: a bounded wait
+// gave up); the host collects and clears it (ra_check_device_errors).
+static __device__ unsigned int g_ra_device_error = 0;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        uint32_t ok;
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                     : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+        if (ok) return true;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 
-template <class E, int NT, int OUT, int MAXSEG>
-__device__ __forceinline__ void fused_vectors(const FusedParams<MAXSEG> &p, int c, int64_t i0, int64_t ae) {
-    constexpr int V = E::kVec;
-    constexpr int VPT = fused_vec_per_thread(NT);
-    const int n = NT > 0 ? NT : p.n;
-    constexpr int esz = (int)sizeof(typename E::T);
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: copies of one tile take microseconds
 
+template <int MAXSEG>
+struct TmaFusedParams {
+    FusedParams<MAXSEG> f;  // rows, aux, w, lr, n, nseg, mis, ntiles, seg
+    int tile_bytes;         // bytes per row per tile (multiple of 16)
+};
+
+// fold one 16-byte vector q over the n staged rows, ring order from row c
+template <class E, int NT, int OUT>
+__device__ __forceinline__ void tma_fold(const unsigned char *stage, int B, int n, int c, int q,
+                                         float (&acc)[E::kVec]) {
+    constexpr int V = E::kVec;
+    float t[V];
+    unpack<E>(reinterpret_cast<const uint4 *>(stage + (size_t)c * B)[q], acc);
     if constexpr (NT > 0) {
-        // all NT x VPT loads issued before any arithmetic
-        uint4 x[VPT][NT];
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t i = i0 + (int64_t)j * kThreads * V;
-            if (i < ae) {
+        for (int k = 1; k < NT; ++k) {
+            const int r = ring_idx(c, k, NT);
+            unpack<E>(reinterpret_cast<const uint4 *>(stage + (size_t)r * B)[q], t);
 #pragma unroll
-                for (int k = 0; k < NT; ++k)
-                    x[j][k] = ld_vec(reinterpret_cast<const char *>(p.rows[ring_idx(c, k, NT)]) + i * esz);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int64_t i = i0 + (int64_t)j * kThreads * V;
-            if (i < ae) {
-                float acc[V], t[V];
-                unpack<E>(x[j][0], acc);
-#pragma unroll
-                for (int k = 1; k < NT; ++k) {
-                    unpack<E>(x[j][k], t);
-#pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        acc[e] = __fadd_rn(t[e], acc[e]);
-                        if constexpr (OUT == kOutAllWire) acc[e] = round_bf16(acc[e]);
-                    }
-                }
-                float avg[V];
-#pragma unroll
-                for (int e = 0; e < V; ++e) avg[e] = div_n<NT>(acc[e], n);
-                fused_emit<E, NT, OUT>(p, c, n, i, avg);
+            for (int e = 0; e < V; ++e) {
+                acc[e] = __fadd_rn(t[e], acc[e]);
+                if constexpr (OUT == kOutAllWire) acc[e] = round_bf16(acc[e]);
             }
         }
     } else {
-        // any n: groups of 8 workers in flight at a time, same fold order
-        constexpr int G = 8;
-        const int64_t i = i0;
-        if (i >= ae) return;
-        float acc[V], t[V];
-        for (int k0 = 0; k0 < n; k0 += G) {
-            uint4 x[G];
+        int r = c;
+        for (int k = 1; k < n; ++k) {
+            r = r + 1 == n ? 0 : r + 1;
+            unpack<E>(reinterpret_cast<const uint4 *>(stage + (size_t)r * B)[q], t);
 #pragma unroll
-            for (int g = 0; g < G; ++g)
-                if (k0 + g < n)
-                    x[g] = ld_vec(reinterpret_cast<const char *>(p.rows[ring_idx(c, k0 + g, n)]) + i * esz);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                if (k0 + g < n) {
-                    if (k0 + g == 0) {
-                        unpack<E>(x[g], acc);
-                    } else {
-                        unpack<E>(x[g], t);
-#pragma unroll
-                        for (int e = 0; e < V; ++e) {
-                            acc[e] = __fadd_rn(t[e], acc[e]);
-                            if constexpr (OUT == kOutAllWire) acc[e] = round_bf16(acc[e]);
-                        }
-                    }
-                }
+            for (int e = 0; e < V; ++e) {
+                acc[e] = __fadd_rn(t[e], acc[e]);
+                if constexpr (OUT == kOutAllWire) acc[e] = round_bf16(acc[e]);
             }
         }
-        float avg[V];
-#pragma unroll
-        for (int e = 0; e < V; ++e) avg[e] = div_n<0>(acc[e], n);
-        fused_emit<E, 0, OUT>(p, c, n, i, avg);
     }
 }
 
-// VECTOR: rows share their 16-byte misalignment (vector interior + scalar
-// edges); otherwise every element takes the scalar path.
-template <class E, int NT, int OUT, bool VECTOR, int MAXSEG>
-__global__ void __launch_bounds__(kThreads) fused_allreduce_kernel(const __grid_constant__ FusedParams<MAXSEG> p) {
+template <class E, int NT, int OUT, int MAXSEG>
+__global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_constant__ TmaFusedParams<MAXSEG> tp) {
     constexpr int V = E::kVec;
+    constexpr int esz = (int)sizeof(typename E::T);
+    const FusedParams<MAXSEG> &p = tp.f;
+    const int n = NT > 0 ? NT : p.n;
+    const int B = tp.tile_bytes;
+    // x / n, or the identical x * (1/n) when n is a power of two (see div_n)
+    const bool pow2 = (n & (n - 1)) == 0;
+    const float inv_n = 1.0f / (float)n;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stage = smem;                      // n rows of B bytes
+    unsigned char *outb = smem + (size_t)n * B;       // B bytes
+    float *wt = reinterpret_cast<float *>(outb + B);  // SGD: the weights of the tile, (B / esz) * 4 bytes
+    const int wbytes_max = OUT == kOutAllSgd ? (B / esz) * 4 : 0;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(outb + B + wbytes_max);
+
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<MAXSEG>(p.seg, p.nseg, tile);
         const Seg sg = p.seg[s];
         const int c = sg.c;
         const int64_t t_in_seg = tile - sg.tile0;
-        if constexpr (VECTOR) {
-            int64_t ab, ae;
-            vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
-            const int64_t i0 = ab + (t_in_seg * fused_tile_vectors(NT) + threadIdx.x) * V;
-            fused_vectors<E, NT, OUT>(p, c, i0, ae);
-            if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) fused_scalar<E, NT, OUT>(p, c, sg.begin + threadIdx.x);
-            const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
-            if (last && threadIdx.x < sg.end - ae) fused_scalar<E, NT, OUT>(p, c, ae + threadIdx.x);
-        } else {
-            const int64_t i0 = sg.begin + t_in_seg * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
-#pragma unroll 4
-            for (int j = 0; j < kScalarPerThread; ++j) {
-                const int64_t i = i0 + (int64_t)j * kThreads;
-                if (i < sg.end) fused_scalar<E, NT, OUT>(p, c, i);
+        int64_t ab, ae;
+        vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
+        const int64_t first = ab + t_in_seg * (B / esz);  // first element of this tile
+        const int64_t left = (ae - first) * esz;
+        const int bytes = left <= 0 ? 0 : (int)(left < B ? left : B);
+        const int wbytes = OUT == kOutAllSgd ? (bytes / esz) * 4 : 0;
+
+        if (bytes > 0) {
+            if (threadIdx.x == 0) {
+                asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_addr(bar)));
+                asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                             :: "r"(smem_addr(bar)), "r"((uint32_t)bytes * (uint32_t)n + (uint32_t)wbytes) : "memory");
+                for (int k = 0; k < n; ++k)
+                    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                                 :: "r"(smem_addr(stage + (size_t)k * B)),
+                                    "l"(reinterpret_cast<const char *>(p.rows[k]) + first * esz), "r"(bytes),
+                                    "r"(smem_addr(bar)) : "memory");
+                if constexpr (OUT == kOutAllSgd)
+                    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                                 :: "r"(smem_addr(wt)), "l"(p.w + first), "r"(wbytes), "r"(smem_addr(bar)) : "memory");
             }
+            __syncthreads();
+            const bool ok = mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
+            if (__syncthreads_or(!ok)) {
+                // the copies never landed: record it, let them finish (bounded), leave
+                if (threadIdx.x == 0) {
+                    atomicOr(&g_ra_device_error, 1u);
+                    mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
+                }
+                __syncthreads();
+                return;
+            }
+            const int nvec = bytes / 16;
+            for (int q = threadIdx.x; q < nvec; q += kThreads) {
+                float acc[V];
+                tma_fold<E, NT, OUT>(stage, B, n, c, q, acc);
+                float avg[V], held[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) avg[e] = pow2 ? __fmul_rn(acc[e], inv_n) : __fdiv_rn(acc[e], (float)n);
+                reinterpret_cast<uint4 *>(outb)[q] = pack<E>(avg, held);
+                if constexpr (OUT == kOutAllSgd) {
+#pragma unroll
+                    for (int e = 0; e < V; e += 4) {
+                        float4 *wp = reinterpret_cast<float4 *>(wt + q * V + e);
+                        float4 wv = *wp;
+                        wv.x = __fsub_rn(wv.x, __fmul_rn(p.lr, held[e + 0]));
+                        wv.y = __fsub_rn(wv.y, __fmul_rn(p.lr, held[e + 1]));
+                        wv.z = __fsub_rn(wv.z, __fmul_rn(p.lr, held[e + 2]));
+                        wv.w = __fsub_rn(wv.w, __fmul_rn(p.lr, held[e + 3]));
+                        *wp = wv;
+                    }
+                }
+            }
+            // generic-proxy writes of the output tile -> visible to the bulk copies
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                if constexpr (OUT == kOutOne) {
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                 :: "l"(reinterpret_cast<char *>(p.aux[c]) + first * esz), "r"(smem_addr(outb)),
+                                    "r"(bytes) : "memory");
+                } else {
+                    for (int k = 0; k < n; ++k)
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                     :: "l"(reinterpret_cast<char *>(p.rows[k]) + first * esz), "r"(smem_addr(outb)),
+                                        "r"(bytes) : "memory");
+                    if constexpr (OUT == kOutAllSgd)
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                     :: "l"(p.w + first), "r"(smem_addr(wt)), "r"(wbytes) : "memory");
+                }
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                // the shared tile must stay valid until the copies have read it
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                asm volatile("mbarrier.inval.shared::cta.b64 [%0];" :: "r"(smem_addr(bar)) : "memory");
+            }
+            __syncthreads();
+        }
+        // ragged head and tail of the segment: scalar path
+        if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) fused_scalar<E, 0, OUT>(p, c, sg.begin + threadIdx.x);
+        const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
+        if (last && threadIdx.x < sg.end - ae) fused_scalar<E, 0, OUT>(p, c, ae + threadIdx.x);
+    }
+}
+
+// Scalar kernel: rows that disagree modulo 16 bytes (no common vector
+// boundary) -- every element through fused_scalar, same fold and rounding.
+template <class E, int OUT, int MAXSEG>
+__global__ void __launch_bounds__(kThreads) fused_scalar_kernel(const __grid_constant__ FusedParams<MAXSEG> p) {
+    for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+        const int s = find_seg<MAXSEG>(p.seg, p.nseg, tile);
+        const Seg sg = p.seg[s];
+        const int64_t i0 = sg.begin + (tile - sg.tile0) * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
+#pragma unroll 4
+        for (int j = 0; j < kScalarPerThread; ++j) {
+            const int64_t i = i0 + (int64_t)j * kThreads;
+            if (i < sg.end) fused_scalar<E, 0, OUT>(p, sg.c, i);
         }
     }
 }

@@ -310,6 +310,28 @@ ra_status ra_reducer_mark_ready(ra_reducer *r, int tensor, void *stream);
 ra_status ra_reducer_finish(ra_reducer *r, void *stream);
 ra_status ra_reducer_destroy(ra_reducer *r);
 
+/*
+ * ra_check_device_errors -- whether a kernel of this library on the current
+ * device gave up a bounded wait since the last check.  The fused kernels
+ * wait for their bulk copies (global -> shared memory) on an mbarrier; each
+ * wait is limited to 2 s (the copies of one tile take microseconds), after
+ * which the kernel records the failure, skips its stores and returns, so the
+ * context stays usable.  Returns RA_ERR_TIMEOUT if such a record exists (the
+ * results of the calls in flight at the time are then invalid), RA_OK
+ * otherwise, and clears the record.  Reads device memory synchronously:
+ * call it after the streams in question have finished.
+ */
+ra_status ra_check_device_errors(void);
+
+/*
+ * ra_selftest_wait_timeout -- exercises that timeout path on purpose: queues
+ * on `stream` a one-block kernel whose mbarrier expects 16 bytes that no copy
+ * delivers; its bounded wait gives up after timeout_us (1 .. 10^7) and
+ * records the failure, so ra_check_device_errors() then returns
+ * RA_ERR_TIMEOUT.  Nothing hangs and no memory is touched.
+ */
+ra_status ra_selftest_wait_timeout(int timeout_us, void *stream);
+
 /* ra_chunk_range -- [begin, end) of chunk c of a p-element array split for
  * n workers (the first p mod n chunks hold one extra element). */
 void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end);
