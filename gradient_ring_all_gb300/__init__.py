@@ -120,8 +120,7 @@ def _dtype_code(t) -> int:
 
 
 def _rows(tensors):
-    """(pointer array, n, p, dtype code) for a list of worker tensors, or raw
-    (pointers, p, dtype) when given ints."""
+    """(pointer array, n, p, dtype code, device) for a list of worker tensors."""
     tensors = list(tensors)
     if not tensors:
         raise ValueError("need at least one worker buffer")
