@@ -37,9 +37,9 @@ bool ranges_disjoint(std::vector<std::pair<uintptr_t, uintptr_t>> r) {
     return true;
 }
 
-// 16-byte vector path: all rows (and the extra pointer, if any, holding
-// binary32 elements indexed like the rows) sit the same number of elements
-// past a 16-byte boundary.
+// 16-byte vector path: all rows sit the same number of elements past a
+// 16-byte boundary (*mis), so one element index starts a vector in all of
+// them.
 bool common_misalignment(void *const *bufs, int n, int dtype, int *mis) {
     const int esz = elem_size(dtype), V = vec_elems(dtype);
     const int m0 = (int)((reinterpret_cast<uintptr_t>(bufs[0]) / esz) % V);
@@ -65,7 +65,7 @@ ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, con
         L.rows[k] = bufs[k];
         L.aux[k] = aux ? aux[k] : nullptr;
     }
-    L.out = bf16_wire ? 3 : (aux ? 2 : (w ? 1 : 0));
+    L.out = bf16_wire ? kOutAllWire : (aux ? kOutOne : (w ? kOutAllSgd : kOutAll));
     L.n = n;
     L.dtype = dtype;
     L.w = w;

@@ -47,10 +47,17 @@ constexpr int kSegLarge = 896;
 
 enum StagedOp { kOpScatter = 0, kOpDivide = 1, kOpGather = 2 };
 
+// Where the fused kernel puts the mean: every worker's array (all-reduce),
+// the same plus the SGD step, or one destination per chunk (reduce-scatter:
+// the worker that owns the chunk, or a separate shard buffer).
+// kOutAllWire: the all-reduce of bf16 arrays with every partial sum rounded
+// to bf16, as a ring that keeps its arrays in bf16 would store them.
+enum FusedOut { kOutAll = 0, kOutAllSgd = 1, kOutOne = 2, kOutAllWire = 3 };
+
 struct FusedLaunch {
     void *rows[RA_MAX_N];
     void *aux[RA_MAX_N];  // reduce-scatter: destination base per chunk
-    int out;              // 0: all workers, 1: + SGD, 2: one destination per chunk, 3: bf16 partials
+    int out;              // FusedOut
     int n;
     int dtype;
     float *w;  // SGD weights

@@ -5,18 +5,23 @@
 // belongs to the same ring chunk c (Gibiansky, "Scatter-Reduce": the array
 // is split into N chunks, and the chunk decides where the scatter-reduce
 // starts accumulating it).  A plain all-reduce has N segments, a bucketed
-// one N per bucket.  Each segment is cut into tiles of 16-byte vectors;
-// every block takes one tile (a grid-stride loop covers grids past the
-// launch limit), finds the tile's segment by binary search in the
-// kernel-parameter table, and so knows c for the whole tile.  The few elements of a segment that do not fill a 16-byte vector
-// (its ragged head and tail) are done with scalar accesses by the
-// segment's first and last tiles.
+// one N per bucket.  Each segment is cut into tiles; every block takes one
+// tile (a grid-stride loop covers grids past the launch limit), finds the
+// tile's segment by binary search in the kernel-parameter table, and so
+// knows c for the whole tile.  The few elements of a segment that do not
+// fill a 16-byte vector (its ragged head and tail) are done with scalar
+// accesses by the segment's first and last tiles.
 //
-// Fused kernel (one pass): for each vector, load the N workers' values in
-// ring order starting at worker c, fold them left in binary32 (the order
-// in which the scatter-reduce adds them), divide by N, and store the mean
-// to all N workers (the all-gather's result).  Loads and stores use the
-// streaming cache hint: every byte is touched exactly once.
+// Kernels:
+//   fused_tma_kernel     the one-pass all-reduce (and its SGD, reduce-scatter
+//                        and bf16-wire variants): TMA bulk copies stage the N
+//                        row tiles in shared memory, the fold runs in ring
+//                        order from worker c in binary32, the mean is divided
+//                        by N and bulk-stored to its destinations;
+//   fused_scalar_kernel  the same arithmetic element by element, for rows
+//                        that share no 16-byte vector boundary;
+//   staged_step_kernel   one iteration of the literal ring per launch;
+//   all_gather_kernel    the all-gather on its own.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -120,12 +125,8 @@ __device__ __forceinline__ float store_scalar_all(void *const *rows, int n, int6
 // nearest even.  For n a power of two, x * (1/n) is the same correctly
 // rounded value (1/n is exact, and both operations round the same real
 // number x/n), so the cheaper multiplication is used there.
-template <int NT>
 __device__ __forceinline__ float div_n(float x, int n) {
-    if constexpr (NT > 0 && (NT & (NT - 1)) == 0)
-        return __fmul_rn(x, 1.0f / (float)NT);
-    else
-        return __fdiv_rn(x, (float)(NT > 0 ? NT : n));
+    return (n & (n - 1)) == 0 ? __fmul_rn(x, 1.0f / (float)n) : __fdiv_rn(x, (float)n);
 }
 
 // worker index (c + k) mod n for 0 <= c, k < n
@@ -137,12 +138,6 @@ __device__ __forceinline__ int ring_idx(int c, int k, int n) {
 // ---------------------------------------------------------------------------
 // segment table
 
-// Where the fused kernel puts the mean: every worker's array (all-reduce),
-// the same plus the SGD step, or one destination per chunk (reduce-scatter:
-// the worker that owns the chunk, or a separate shard buffer).
-// kOutAllWire: the all-reduce of bf16 arrays with every partial sum rounded
-// to bf16, as a ring that keeps its arrays in bf16 would store them.
-enum FusedOut { kOutAll = 0, kOutAllSgd = 1, kOutOne = 2, kOutAllWire = 3 };
 
 // binary32 value of the nearest bf16 (ties to even)
 __device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_f32(f32_to_bf16_bits(x)); }
@@ -178,15 +173,15 @@ __device__ __forceinline__ int find_seg(const Seg *seg, int nseg, int64_t tile) 
 // fused kernel
 
 // one element through the scalar path: ring-order fold from worker c
-template <class E, int NT, int OUT, int MAXSEG>
+template <class E, int OUT, int MAXSEG>
 __device__ __forceinline__ void fused_scalar(const FusedParams<MAXSEG> &p, int c, int64_t i) {
-    const int n = NT > 0 ? NT : p.n;
+    const int n = p.n;
     float acc = load_scalar<E>(p.rows[c], i);
     for (int k = 1; k < n; ++k) {
         acc = __fadd_rn(load_scalar<E>(p.rows[ring_idx(c, k, n)], i), acc);
         if constexpr (OUT == kOutAllWire) acc = round_bf16(acc);
     }
-    const float avg = div_n<NT>(acc, n);
+    const float avg = div_n(acc, n);
     if constexpr (OUT == kOutOne) {
         store_scalar_all<E>(&p.aux[c], 1, i, avg);
     } else {
@@ -278,9 +273,6 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
     const FusedParams<MAXSEG> &p = tp.f;
     const int n = NT > 0 ? NT : p.n;
     const int B = tp.tile_bytes;
-    // x / n, or the identical x * (1/n) when n is a power of two (see div_n)
-    const bool pow2 = (n & (n - 1)) == 0;
-    const float inv_n = 1.0f / (float)n;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char *stage = smem;                      // n rows of B bytes
     unsigned char *outb = smem + (size_t)n * B;       // B bytes
@@ -332,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
                 tma_fold<E, NT, OUT>(stage, B, n, c, q, acc);
                 float avg[V], held[V];
 #pragma unroll
-                for (int e = 0; e < V; ++e) avg[e] = pow2 ? __fmul_rn(acc[e], inv_n) : __fdiv_rn(acc[e], (float)n);
+                for (int e = 0; e < V; ++e) avg[e] = div_n(acc[e], n);
                 reinterpret_cast<uint4 *>(outb)[q] = pack<E>(avg, held);
                 if constexpr (OUT == kOutAllSgd) {
 #pragma unroll
@@ -372,9 +364,9 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
             __syncthreads();
         }
         // ragged head and tail of the segment: scalar path
-        if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) fused_scalar<E, 0, OUT>(p, c, sg.begin + threadIdx.x);
+        if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) fused_scalar<E, OUT>(p, c, sg.begin + threadIdx.x);
         const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
-        if (last && threadIdx.x < sg.end - ae) fused_scalar<E, 0, OUT>(p, c, ae + threadIdx.x);
+        if (last && threadIdx.x < sg.end - ae) fused_scalar<E, OUT>(p, c, ae + threadIdx.x);
     }
 }
 
@@ -389,7 +381,7 @@ __global__ void __launch_bounds__(kThreads) fused_scalar_kernel(const __grid_con
 #pragma unroll 4
         for (int j = 0; j < kScalarPerThread; ++j) {
             const int64_t i = i0 + (int64_t)j * kThreads;
-            if (i < sg.end) fused_scalar<E, 0, OUT>(p, sg.c, i);
+            if (i < sg.end) fused_scalar<E, OUT>(p, sg.c, i);
         }
     }
 }
