@@ -194,6 +194,21 @@ def _cpu_oracle_sample(n: int, p: int, reps: int):
     return 2.0 * n * p * 4 * reps / dt / 1e9, dt
 
 
+def _oracle_step(wl, rows, w, plan):
+    """One oracle run of the workload's call on host rows, in place."""
+    import oracle
+    if plan:
+        for off, cnt in plan:
+            sub = [r[off:off + cnt] for r in rows]
+            (oracle.ring_allreduce_avg_f32 if wl.dtype == "f32" else oracle.ring_allreduce_avg_bf16)(sub)
+    elif wl.dtype == "f32":
+        oracle.ring_allreduce_avg_f32(rows)
+    else:
+        oracle.ring_allreduce_avg_bf16(rows)
+    if w is not None:
+        oracle.sgd_update_f32(w, rows[0], wl.sgd_lr)
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -202,27 +217,40 @@ def run_reference(args):
     import synth
     oracle.build()
     synth.build()
-    wl = synth.WORKLOADS[WORKLOAD]
-    # per-step sample sized so that all W + K steps take about a minute
-    # (one 25M-element step is about 0.6 s of one core)
-    p = int(min(CPU_SAMPLE_P, max(1_000_000, CPU_SAMPLE_P * 100 // (args.steps + args.warmup))))
-    rows = [synth.normal_f32(wl.seed, k, wl.scale, 0, p) for k in range(wl.n)]
+    wl = synth.WORKLOADS[args.workload]
+    esz = 4 if wl.dtype == "f32" else 2
+    # per-step sample: at most 8 x 25M values (about 0.6 s of one core), fewer
+    # when W + K steps would otherwise take more than about a minute
+    values = min(8 * CPU_SAMPLE_P, 8 * CPU_SAMPLE_P * 100 // (args.steps + args.warmup))
+    p = int(min(wl.p, max(1_000_000 // wl.n, values // wl.n)))
+    rows = [wl.row(k, 0, p) for k in range(wl.n)]
+    w = wl.weights(0, p) if wl.sgd_lr > 0 else None
+    plan = None
+    if wl.bucket_cap_bytes:
+        # the workload's reverse-order buckets over the first p elements
+        numel, left = [], p
+        for t in wl.tensors:
+            if left <= 0:
+                break
+            numel.append(min(t, left))
+            left -= numel[-1]
+        plan = oracle.bucket_plan(numel, esz, wl.bucket_cap_bytes)
     for _ in range(args.warmup):
-        oracle.ring_allreduce_avg_f32(rows)
+        _oracle_step(wl, rows, w, plan)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.ring_allreduce_avg_f32(rows)
+        _oracle_step(wl, rows, w, plan)
         times.append(time.perf_counter() - t0)
     total = sum(times)
-    value = 2.0 * wl.n * p * 4 * args.steps / total / 1e9
-    sample = "ring of N=%d x P=%d fp32 elements (N(0,%g), seed %d) per step, in place" % (
-        wl.n, p, wl.scale, wl.seed)
+    nbytes = 2 * wl.n * p * esz + (2 * p * 4 if w is not None else 0)
+    value = nbytes * args.steps / total / 1e9
+    sample = "N=%d workers x P=%d %s elements of %s per step, in place" % (wl.n, p, wl.dtype, wl.name)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "workers": wl.n, "elements_per_worker": p,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic", "config": {"workload": wl.name, "workers": wl.n, "elements_per_worker": p,
                                         "note": "CPU oracle on a bounded sample of the workload"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
