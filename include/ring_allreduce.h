@@ -58,7 +58,7 @@ typedef enum { RA_F32 = 0, RA_BF16 = 1 } ra_dtype;
 typedef enum {
     RA_OK = 0,
     RA_ERR_INVALID_ARG = 1, /* null pointer, n out of range, p < 0, bad dtype, misaligned element */
-    RA_ERR_UNSUPPORTED = 2, /* a valid request this build does not implement */
+    RA_ERR_UNSUPPORTED = 2, /* a valid request outside what the called function handles (see its notes) */
     RA_ERR_OVERLAP = 3,     /* two buffers (or w and a buffer) share bytes */
     RA_ERR_CUDA = 4,        /* a CUDA call failed; see ra_last_cuda_error() */
     RA_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait gave up */
