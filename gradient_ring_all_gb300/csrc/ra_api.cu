@@ -436,7 +436,8 @@ ra_status ra_all_gather(void *const *bufs, int n, int64_t p, int dtype, void *co
     if (st != RA_OK) return st;
     std::vector<Seg> segs;
     ring_segments(0, p, n, &segs);
-    L.ntiles = staged_assign_tiles(segs.data(), (int)segs.size(), dtype, L.vector, mis);
+    L.ntiles = L.vector ? fused_tma_assign_tiles(segs.data(), (int)segs.size(), dtype, mis, kGatherTileBytes)
+                        : staged_assign_tiles(segs.data(), (int)segs.size(), dtype, false, mis);
     L.seg = segs.data();
     L.nseg = (int)segs.size();
     cudaError_t e = launch_all_gather(L, static_cast<cudaStream_t>(stream));

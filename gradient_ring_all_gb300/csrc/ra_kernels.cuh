@@ -21,7 +21,9 @@
 //   fused_scalar_kernel  the same arithmetic element by element, for rows
 //                        that share no 16-byte vector boundary;
 //   staged_step_kernel   one iteration of the literal ring per launch;
-//   all_gather_kernel    the all-gather on its own.
+//   all_gather_tma_kernel / all_gather_scalar_kernel
+//                        the all-gather on its own (bulk copies through
+//                        shared memory, or element by element).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -559,44 +561,75 @@ __device__ __forceinline__ void gather_scalar(const GatherParams &p, int c, int6
         if (!(p.skip_owner && k == owner)) reinterpret_cast<T *>(p.rows[k])[i] = v;
 }
 
-template <class E, bool VEC>
-__global__ void __launch_bounds__(kThreads) all_gather_kernel(const __grid_constant__ GatherParams p) {
+// scalar all-gather, for rows (or shards) that share no 16-byte boundary
+template <class E>
+__global__ void __launch_bounds__(kThreads) all_gather_scalar_kernel(const __grid_constant__ GatherParams p) {
+    for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+        const int s = find_seg<RA_MAX_N>(p.seg, p.nseg, tile);
+        const Seg sg = p.seg[s];
+        const int64_t i0 = sg.begin + (tile - sg.tile0) * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
+        for (int j = 0; j < kScalarPerThread; ++j) {
+            const int64_t i = i0 + (int64_t)j * kThreads;
+            if (i < sg.end) gather_scalar<E>(p, sg.c, i);
+        }
+    }
+}
+
+// TMA all-gather: thread 0 of a one-warp block bulk-copies the owner's tile
+// of chunk c into shared memory and bulk-stores it to every destination row;
+// no arithmetic, so the copy engine does all the work.  The other lanes only
+// take the scalar head and tail.
+template <class E>
+__global__ void __launch_bounds__(32) all_gather_tma_kernel(const __grid_constant__ GatherParams p, int tile_bytes) {
     constexpr int V = E::kVec;
     constexpr int esz = (int)sizeof(typename E::T);
+    const int B = tile_bytes;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + B);
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<RA_MAX_N>(p.seg, p.nseg, tile);
         const Seg sg = p.seg[s];
         const int c = sg.c;
         const int owner = c == 0 ? p.n - 1 : c - 1;
         const int64_t t_in_seg = tile - sg.tile0;
-        if constexpr (VEC) {
-            int64_t ab, ae;
-            vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
-            const int64_t i0 = ab + (t_in_seg * kStagedTileVec + threadIdx.x) * V;
-            constexpr int J = kStagedTileVec / kThreads;
-            uint4 v[J];
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int64_t i = i0 + (int64_t)j * kThreads * V;
-                if (i < ae) v[j] = ld_vec(reinterpret_cast<const char *>(p.src[c]) + i * esz);
-            }
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int64_t i = i0 + (int64_t)j * kThreads * V;
-                if (i < ae)
-                    for (int k = 0; k < p.n; ++k)
-                        if (!(p.skip_owner && k == owner)) st_vec(reinterpret_cast<char *>(p.rows[k]) + i * esz, v[j]);
-            }
-            if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) gather_scalar<E>(p, c, sg.begin + threadIdx.x);
-            const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
-            if (last && threadIdx.x < sg.end - ae) gather_scalar<E>(p, c, ae + threadIdx.x);
-        } else {
-            const int64_t i0 = sg.begin + t_in_seg * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
-            for (int j = 0; j < kScalarPerThread; ++j) {
-                const int64_t i = i0 + (int64_t)j * kThreads;
-                if (i < sg.end) gather_scalar<E>(p, c, i);
-            }
+        int64_t ab, ae;
+        vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
+        const int64_t first = ab + t_in_seg * (B / esz);
+        const int64_t left = (ae - first) * esz;
+        const int bytes = left <= 0 ? 0 : (int)(left < B ? left : B);
+        int fail = 0;
+        if (bytes > 0 && threadIdx.x == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_addr(bar)));
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                         :: "r"(smem_addr(bar)), "r"((uint32_t)bytes) : "memory");
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         :: "r"(smem_addr(smem)), "l"(reinterpret_cast<const char *>(p.src[c]) + first * esz),
+                            "r"(bytes), "r"(smem_addr(bar)) : "memory");
+            fail = mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs) ? 0 : 1;
         }
+        // the whole warp leaves together if the copy never landed
+        if (__shfl_sync(0xffffffffu, fail, 0)) {
+            if (threadIdx.x == 0) {
+                atomicOr(&g_ra_device_error, 1u);
+                mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
+            }
+            return;
+        }
+        if (bytes > 0 && threadIdx.x == 0) {
+            for (int k = 0; k < p.n; ++k)
+                if (!(p.skip_owner && k == owner))
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                 :: "l"(reinterpret_cast<char *>(p.rows[k]) + first * esz), "r"(smem_addr(smem)),
+                                    "r"(bytes) : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            asm volatile("mbarrier.inval.shared::cta.b64 [%0];" :: "r"(smem_addr(bar)) : "memory");
+        }
+        if (t_in_seg == 0 && threadIdx.x < ab - sg.begin) gather_scalar<E>(p, c, sg.begin + threadIdx.x);
+        const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
+        if (last && threadIdx.x < sg.end - ae) gather_scalar<E>(p, c, ae + threadIdx.x);
+        __syncwarp();
     }
 }
 

@@ -31,8 +31,8 @@ cudaError_t launch_staged_step(const StagedLaunch &L, int op, int t, cudaStream_
     return L.vector ? staged_launch_one<BF16, true>(L, op, t, s) : staged_launch_one<BF16, false>(L, op, t, s);
 }
 
-template <class E, bool VEC>
-static cudaError_t gather_launch_one(const GatherLaunch &L, cudaStream_t s) {
+template <class E>
+static cudaError_t gather_scalar_launch(const GatherLaunch &L, cudaStream_t s) {
     GatherParams p;
     memset(&p, 0, sizeof(p));
     for (int k = 0; k < L.n; ++k) {
@@ -46,15 +46,45 @@ static cudaError_t gather_launch_one(const GatherLaunch &L, cudaStream_t s) {
     p.ntiles = L.ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
     const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
-    all_gather_kernel<E, VEC><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    all_gather_scalar_kernel<E><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <class E>
+static cudaError_t gather_tma_launch(const GatherLaunch &L, cudaStream_t s) {
+    GatherParams p;
+    memset(&p, 0, sizeof(p));
+    for (int k = 0; k < L.n; ++k) {
+        p.rows[k] = L.rows[k];
+        p.src[k] = L.src[k];
+    }
+    p.n = L.n;
+    p.nseg = L.nseg;
+    p.mis = L.mis;
+    p.skip_owner = L.skip_owner ? 1 : 0;
+    p.ntiles = L.ntiles;
+    for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
+    const size_t smem = (size_t)kGatherTileBytes + 16;
+    if (smem > 48 * 1024) {
+        static unsigned long long opted_in = 0;  // bit per device
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 64 && !(__atomic_load_n(&opted_in, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+            e = cudaFuncSetAttribute(all_gather_tma_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            __atomic_fetch_or(&opted_in, 1ull << dev, __ATOMIC_ACQ_REL);
+        }
+    }
+    const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
+    all_gather_tma_kernel<E><<<(unsigned)grid, 32, smem, s>>>(p, kGatherTileBytes);
     return cudaGetLastError();
 }
 
 cudaError_t launch_all_gather(const GatherLaunch &L, cudaStream_t s) {
     if (L.nseg > RA_MAX_N) return cudaErrorInvalidValue;
-    if (L.dtype == RA_F32)
-        return L.vector ? gather_launch_one<F32, true>(L, s) : gather_launch_one<F32, false>(L, s);
-    return L.vector ? gather_launch_one<BF16, true>(L, s) : gather_launch_one<BF16, false>(L, s);
+    if (L.vector) return L.dtype == RA_F32 ? gather_tma_launch<F32>(L, s) : gather_tma_launch<BF16>(L, s);
+    return L.dtype == RA_F32 ? gather_scalar_launch<F32>(L, s) : gather_scalar_launch<BF16>(L, s);
 }
 
 }  // namespace ra
