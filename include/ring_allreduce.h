@@ -31,7 +31,12 @@
  *     is read during the call only.  The buffers must not overlap.
  *   - All device memory is owned by the caller and must stay valid until
  *     the work queued on `stream` has finished.  Calls are asynchronous on
- *     `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream): they only
+ *     queue kernels and return.  One exception is the first launch of each
+ *     kernel variant in a process, which loads its module; with CUDA's lazy
+ *     module loading (the default) that load may synchronise the context,
+ *     so warm a call up once (or set CUDA_MODULE_LOADING=EAGER) before
+ *     relying on overlap.
  *   - Arguments are checked before anything is queued; a non-OK status
  *     means nothing was launched.  RA_ERR_CUDA reports a failed launch or
  *     device query; ra_last_cuda_error() returns its cudaError_t value.
