@@ -73,7 +73,7 @@ ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, con
     L.vector = vector;
     L.mis = mis;
     std::vector<Seg> tab(segs, segs + nseg);
-    L.tile_bytes = fused_tile_bytes(n);
+    L.tile_bytes = fused_tile_bytes(n, L.out == kOutOne);
     const int64_t ntiles = vector ? fused_tma_assign_tiles(tab.data(), nseg, dtype, mis, L.tile_bytes)
                                   : fused_scalar_assign_tiles(tab.data(), nseg);
     L.seg = tab.data();
