@@ -77,3 +77,74 @@ def test_bad_arguments_are_rejected_before_any_launch(lib):
     # p == 0 and n == 1 are no-ops that succeed without touching the device
     assert lib.ra_allreduce_avg(bufs, 4, 0, 0, None) == 0
     assert lib.ra_allreduce_avg(bufs, 1, 10, 0, None) == 0
+
+
+def test_every_call_rejects_bad_arguments_on_the_host(lib):
+    # fake, never-dereferenced addresses: each case fails an argument check
+    # before the library touches CUDA
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    P = ctypes.POINTER
+    INVALID, UNSUPPORTED, OVERLAP = 1, 2, 3
+    F32, BF16 = 0, 1
+    rows = (vp * 4)(0x100000, 0x200000, 0x300000, 0x400000)   # 1 MiB apart
+    # every case below must fail its argument check: none may reach a launch
+    p = 1000
+
+    lib.ra_reduce_scatter_avg.argtypes = [P(vp), ctypes.c_int, i64, ctypes.c_int, P(vp), vp]
+    lib.ra_all_gather.argtypes = [P(vp), ctypes.c_int, i64, ctypes.c_int, P(vp), vp]
+    # shards: shard m holds chunk (m+1) mod 4 of 250 elements
+    ov = (vp * 4)(0x900000, 0x900000 + 400, 0xA00000, 0xB00000)      # first two overlap
+    assert lib.ra_reduce_scatter_avg(rows, 4, p, F32, ov, None) == OVERLAP
+    assert lib.ra_all_gather(rows, 4, p, F32, ov, None) == OVERLAP
+    into_rows = (vp * 4)(0x100000 + 64, 0xA00000, 0xB00000, 0xC00000)  # inside worker 0's array
+    assert lib.ra_reduce_scatter_avg(rows, 4, p, F32, into_rows, None) == OVERLAP
+    odd = (vp * 4)(0x900001, 0xA00000, 0xB00000, 0xC00000)             # not element-aligned
+    assert lib.ra_reduce_scatter_avg(rows, 4, p, F32, odd, None) == INVALID
+    nul = (vp * 4)(0, 0xA00000, 0xB00000, 0xC00000)
+    assert lib.ra_all_gather(rows, 4, p, F32, nul, None) == INVALID
+
+    class Bucket(ctypes.Structure):
+        _fields_ = [("offset", i64), ("count", i64)]
+    lib.ra_allreduce_avg_buckets.argtypes = [P(vp), ctypes.c_int, ctypes.c_int, P(Bucket), ctypes.c_int, vp]
+    b = (Bucket * 2)(Bucket(0, 600), Bucket(500, 100))                  # overlap
+    assert lib.ra_allreduce_avg_buckets(rows, 4, F32, b, 2, None) == OVERLAP
+    b = (Bucket * 1)(Bucket(-1, 10))
+    assert lib.ra_allreduce_avg_buckets(rows, 4, F32, b, 1, None) == INVALID
+    b = (Bucket * 1)(Bucket(0, 300000))                                 # 1.2 MB rows, 1 MiB apart: overlap
+    assert lib.ra_allreduce_avg_buckets(rows, 4, F32, b, 1, None) == OVERLAP
+
+    class Traffic(ctypes.Structure):
+        _fields_ = [("sent", i64), ("received", i64)]
+    lib.ra_allreduce_avg_staged.argtypes = [P(vp), ctypes.c_int, i64, ctypes.c_int, vp, ctypes.c_size_t,
+                                            P(Traffic), vp]
+    lib.ra_staged_workspace_bytes.restype = ctypes.c_size_t
+    need = lib.ra_staged_workspace_bytes(4, i64(p), BF16)
+    assert lib.ra_allreduce_avg_staged(rows, 4, p, BF16, vp(0x900000), need - 1, None, None) == INVALID
+    assert lib.ra_allreduce_avg_staged(rows, 4, p, BF16, None, need, None, None) == INVALID
+    assert lib.ra_allreduce_avg_staged(rows, 4, p, BF16, vp(0x200000 + 16), need, None, None) == OVERLAP
+
+    lib.ra_allreduce_avg_staged_static.argtypes = [P(vp), ctypes.c_int, i64, ctypes.c_int, P(Traffic), vp]
+    far = (vp * 2)(0x10000000, 0x20000000)
+    assert lib.ra_allreduce_avg_staged_static(far, 2, 4194304 + 1, BF16, None, None) == UNSUPPORTED
+
+    lib.ra_allreduce_avg_host.argtypes = [P(vp), P(vp), ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, vp]
+    assert lib.ra_allreduce_avg_host(rows, None, 4, p, F32, 7, None) == INVALID     # mode
+    assert lib.ra_allreduce_avg_host(None, None, 4, p, F32, 0, None) == INVALID
+
+    lib.ra_reducer_create.argtypes = [P(vp), ctypes.c_int, ctypes.c_int, P(i64), ctypes.c_int, i64, P(vp)]
+    h = vp()
+    numel = (i64 * 2)(400, 600)
+    assert lib.ra_reducer_create(rows, 4, F32, numel, 2, 0, ctypes.byref(h)) == INVALID          # cap
+    assert lib.ra_reducer_create(rows, 4, 9, numel, 2, 1024, ctypes.byref(h)) == INVALID          # dtype
+    big = (i64 * 2)(400, 300000)
+    assert lib.ra_reducer_create(rows, 4, F32, big, 2, 1024, ctypes.byref(h)) == OVERLAP          # rows overlap
+    assert lib.ra_reducer_create(rows, 4, F32, numel, 2, 1024, None) == INVALID
+
+    lib.ra_bucket_plan.argtypes = [P(i64), ctypes.c_int, ctypes.c_int, i64, P(Bucket), ctypes.c_int,
+                                   P(ctypes.c_int)]
+    out = (Bucket * 1)()
+    nb = ctypes.c_int(0)
+    three = (i64 * 3)(100, 100, 100)
+    assert lib.ra_bucket_plan(three, 3, 4, 400, out, 1, ctypes.byref(nb)) == INVALID              # max_out too small
+    lib.ra_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
+    assert lib.ra_selftest_wait_timeout(0, None) == INVALID
