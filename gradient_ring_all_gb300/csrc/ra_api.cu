@@ -75,7 +75,7 @@ ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, con
     std::vector<Seg> tab(segs, segs + nseg);
     L.tile_bytes = fused_tile_bytes(n, L.out == kOutOne);
     const int64_t ntiles = vector ? fused_tma_assign_tiles(tab.data(), nseg, dtype, mis, L.tile_bytes)
-                                  : fused_scalar_assign_tiles(tab.data(), nseg);
+                                  : fused_unaligned_assign_tiles(tab.data(), nseg, dtype, L.tile_bytes);
     L.seg = tab.data();
     L.nseg = nseg;
     if (ntiles == 0) return RA_OK;
@@ -138,12 +138,14 @@ ra_status check_rows(void *const *bufs, int n, int64_t p, int dtype) {
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
 
-int64_t fused_scalar_assign_tiles(Seg *seg, int nseg) {
-    const int64_t ts = (int64_t)kThreadsPerBlock * kScalarPerThread;
+int64_t fused_unaligned_assign_tiles(Seg *seg, int nseg, int dtype, int tile_bytes) {
+    const int V = vec_elems(dtype), esz = elem_size(dtype);
     int64_t t = 0;
     for (int k = 0; k < nseg; ++k) {
         seg[k].tile0 = t;
-        t += std::max<int64_t>(1, (seg[k].end - seg[k].begin + ts - 1) / ts);
+        int64_t ab, ae;
+        unaligned_interior(seg[k].begin, seg[k].end, V, &ab, &ae);
+        t += std::max<int64_t>(1, ((ae - ab) * esz + tile_bytes - 1) / tile_bytes);
     }
     return t;
 }

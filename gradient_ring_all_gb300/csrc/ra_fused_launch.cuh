@@ -9,10 +9,8 @@
 
 namespace ra {
 
-// scalar path (rows that disagree modulo 16 bytes): element by element
 template <class E, int OUT, int MAXSEG>
-static cudaError_t fused_scalar_launch_one(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
-    FusedParams<MAXSEG> p;
+static void fill_params(FusedParams<MAXSEG> &p, const FusedLaunch &L, int64_t ntiles) {
     memset(&p, 0, sizeof(p));
     for (int k = 0; k < L.n; ++k) {
         p.rows[k] = L.rows[k];
@@ -25,6 +23,34 @@ static cudaError_t fused_scalar_launch_one(const FusedLaunch &L, int64_t ntiles,
     p.mis = L.mis;
     p.ntiles = ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
+}
+
+// large dynamic shared memory needs an opt-in per kernel and device
+template <class K>
+static cudaError_t opt_in_smem(K kern, unsigned long long *opted_in) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !(__atomic_load_n(opted_in, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(opted_in, 1ull << dev, __ATOMIC_ACQ_REL);
+    }
+    return cudaSuccess;
+}
+
+// rows that disagree modulo 16 bytes: the TMA kernel with widened copies
+template <class E, int OUT, int MAXSEG>
+static cudaError_t fused_unaligned_launch_one(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+    auto kern = fused_tma_unaligned_kernel<E, OUT, MAXSEG>;
+    static unsigned long long opted_in = 0;  // bit per device
+    cudaError_t e = opt_in_smem(kern, &opted_in);
+    if (e != cudaSuccess) return e;
+    TmaFusedParams<MAXSEG> tp;
+    fill_params<E, OUT, MAXSEG>(tp.f, L, ntiles);
+    tp.tile_bytes = L.tile_bytes;
+    const size_t smem = unaligned_smem_bytes(L.n, L.tile_bytes);
+    if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;
     // One tile per block.  The block scheduler hands out blocks in index
     // order, so the tiles in flight form one contiguous address window that
     // slides through the arrays; that keeps DRAM pages open far better than
@@ -32,59 +58,40 @@ static cudaError_t fused_scalar_launch_one(const FusedLaunch &L, int64_t ntiles,
     // 6.28 TB/s at N=8, P=300M f32).  The kernel's tile loop only matters
     // past 2^31-1 tiles.
     const int64_t grid = ntiles < kMaxGrid ? ntiles : kMaxGrid;
-    fused_scalar_kernel<E, OUT, MAXSEG><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
+    kern<<<(unsigned)grid, kThreadsPerBlock, smem, s>>>(tp);
     return cudaGetLastError();
 }
 
 template <class E>
-static cudaError_t fused_scalar_dispatch(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
+static cudaError_t fused_unaligned_dispatch(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     const bool big = L.nseg > kSegSmall;
     if (L.out != kOutAll && big) return cudaErrorInvalidValue;
     switch (L.out) {
-        case kOutAllSgd: return fused_scalar_launch_one<E, kOutAllSgd, kSegSmall>(L, ntiles, s);
-        case kOutOne: return fused_scalar_launch_one<E, kOutOne, kSegSmall>(L, ntiles, s);
+        case kOutAllSgd: return fused_unaligned_launch_one<E, kOutAllSgd, kSegSmall>(L, ntiles, s);
+        case kOutOne: return fused_unaligned_launch_one<E, kOutOne, kSegSmall>(L, ntiles, s);
         case kOutAllWire:
             if constexpr (sizeof(typename E::T) == 2)
-                return fused_scalar_launch_one<E, kOutAllWire, kSegSmall>(L, ntiles, s);
+                return fused_unaligned_launch_one<E, kOutAllWire, kSegSmall>(L, ntiles, s);
             return cudaErrorInvalidValue;
         default:
-            if (big) return fused_scalar_launch_one<E, kOutAll, kSegLarge>(L, ntiles, s);
-            return fused_scalar_launch_one<E, kOutAll, kSegSmall>(L, ntiles, s);
+            if (big) return fused_unaligned_launch_one<E, kOutAll, kSegLarge>(L, ntiles, s);
+            return fused_unaligned_launch_one<E, kOutAll, kSegSmall>(L, ntiles, s);
     }
 }
 
 template <class E, int NT, int OUT, int MAXSEG>
 static cudaError_t fused_tma_launch_one(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     auto kern = fused_tma_kernel<E, NT, OUT, MAXSEG>;
-    // large dynamic shared memory needs an opt-in per kernel and device
     static unsigned long long opted_in = 0;  // bit per device
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = opt_in_smem(kern, &opted_in);
     if (e != cudaSuccess) return e;
-    if (dev < 64 && !(__atomic_load_n(&opted_in, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
-        if (e != cudaSuccess) return e;
-        __atomic_fetch_or(&opted_in, 1ull << dev, __ATOMIC_ACQ_REL);
-    }
     TmaFusedParams<MAXSEG> tp;
-    memset(&tp, 0, sizeof(tp));
-    FusedParams<MAXSEG> &p = tp.f;
-    for (int k = 0; k < L.n; ++k) {
-        p.rows[k] = L.rows[k];
-        p.aux[k] = L.aux[k];
-    }
-    p.w = L.w;
-    p.lr = L.lr;
-    p.n = L.n;
-    p.nseg = L.nseg;
-    p.mis = L.mis;
-    p.ntiles = ntiles;
-    for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
+    fill_params<E, OUT, MAXSEG>(tp.f, L, ntiles);
     tp.tile_bytes = L.tile_bytes;
     const int esz = (int)sizeof(typename E::T);
     const size_t smem = (size_t)L.n * L.tile_bytes + L.tile_bytes + (OUT == kOutAllSgd ? L.tile_bytes / esz * 4 : 0) + 16;
     if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;
-    // one tile per block (see fused_scalar_launch_one)
+    // one tile per block (see fused_unaligned_launch_one)
     const int64_t grid = ntiles < kMaxGrid ? ntiles : kMaxGrid;
     kern<<<(unsigned)grid, kThreadsPerBlock, smem, s>>>(tp);
     return cudaGetLastError();
@@ -139,7 +146,7 @@ static cudaError_t collect_device_error(unsigned int *flags) {
 
 template <class E>
 static cudaError_t fused_launch_dtype(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
-    return L.vector ? fused_tma_dispatch<E>(L, ntiles, s) : fused_scalar_dispatch<E>(L, ntiles, s);
+    return L.vector ? fused_tma_dispatch<E>(L, ntiles, s) : fused_unaligned_dispatch<E>(L, ntiles, s);
 }
 
 }  // namespace ra

@@ -23,7 +23,7 @@ static_assert(sizeof(Seg) == 32, "Seg layout");
 
 constexpr int kThreadsPerBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;  // largest gridDim.x
-constexpr int kScalarPerThread = 4;  // elements per thread per tile, scalar path
+constexpr int kScalarPerThread = 4;  // elements per thread per tile, scalar staged and gather paths
 constexpr int kStagedTileVec = 512;  // 16-byte vectors per tile, staged kernel
 
 // The 16-byte-vector interior [ab, ae) of the element range [b, e) when the
@@ -96,14 +96,28 @@ constexpr int kMaxDynamicSmem = 227 * 1024;
 
 int64_t fused_tma_assign_tiles(Seg *seg, int nseg, int dtype, int mis, int tile_bytes);
 
+// Rows that disagree modulo 16 bytes: the bulk-copied part of a segment
+// keeps one 16-byte vector of elements away from each end, so the copies,
+// widened to 16-byte boundaries, stay inside the segment.  The margins (and
+// segments too short to have an interior) are done element by element.
+__host__ __device__ inline void unaligned_interior(int64_t b, int64_t e, int V, int64_t *ab, int64_t *ae) {
+    *ab = b + V;
+    *ae = e - V;
+    if (*ae < *ab) *ab = *ae = b;
+}
+// shared memory of the unaligned kernel: a slot of B + 16 bytes per row
+// (room for the widening), the mbarrier, and the per-row byte offsets
+inline size_t unaligned_smem_bytes(int n, int tile_bytes) {
+    return (size_t)n * (tile_bytes + 16) + 16 + (size_t)n * sizeof(int);
+}
+int64_t fused_unaligned_assign_tiles(Seg *seg, int nseg, int dtype, int tile_bytes);
+
 // collect and clear the device error flags of the fused-kernel translation units
 cudaError_t collect_device_error_f32(unsigned int *flags);
 cudaError_t collect_device_error_bf16(unsigned int *flags);
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t s);
 
-// fill seg[].tile0 and return the tile count: fused scalar kernel, staged
-// kernel, fused TMA kernel
-int64_t fused_scalar_assign_tiles(Seg *seg, int nseg);
+// fill seg[].tile0 and return the tile count of the staged kernel
 int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis);
 
 cudaError_t launch_fused_f32(const FusedLaunch &L, int64_t ntiles, cudaStream_t s);

@@ -18,8 +18,10 @@
 //                        row tiles in shared memory, the fold runs in ring
 //                        order from worker c in binary32, the mean is divided
 //                        by N and bulk-stored to its destinations;
-//   fused_scalar_kernel  the same arithmetic element by element, for rows
-//                        that share no 16-byte vector boundary;
+//   fused_tma_unaligned_kernel
+//                        the same for rows that share no 16-byte vector
+//                        boundary: each row's tile is copied widened to
+//                        16-byte boundaries and read at its own offset;
 //   staged_step_kernel   one iteration of the literal ring per launch;
 //   all_gather_tma_kernel / all_gather_scalar_kernel
 //                        the all-gather on its own (bulk copies through
@@ -372,19 +374,102 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
     }
 }
 
-// Scalar kernel: rows that disagree modulo 16 bytes (no common vector
-// boundary) -- every element through fused_scalar, same fold and rounding.
+// TMA kernel for rows that disagree modulo 16 bytes.  A bulk copy needs a
+// 16-byte-aligned source, so for each row thread 0 copies the aligned span
+// that covers the tile -- from the tile's first byte rounded down to the
+// end rounded up -- and the row's elements start d_k bytes into its staging
+// slot.  Threads read the staged values with scalar shared-memory loads,
+// fold them in ring order, and store the mean with scalar stores that are
+// coalesced across the warp.  Tiles keep 16 bytes away from both ends of
+// their segment (those elements take the scalar path), so the widened
+// copies never leave the segment's own bytes.
 template <class E, int OUT, int MAXSEG>
-__global__ void __launch_bounds__(kThreads) fused_scalar_kernel(const __grid_constant__ FusedParams<MAXSEG> p) {
+__global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __grid_constant__ TmaFusedParams<MAXSEG> tp) {
+    using T = typename E::T;
+    constexpr int V = E::kVec;
+    constexpr int esz = (int)sizeof(T);
+    const FusedParams<MAXSEG> &p = tp.f;
+    const int n = p.n;
+    const int B = tp.tile_bytes;          // bytes of each row per tile
+    const int slot = B + 16;              // staging slot per row: room for the widening
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)n * slot);
+    int *shift = reinterpret_cast<int *>(smem + (size_t)n * slot + 16);  // d_k: where row k's tile starts in its slot
+
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<MAXSEG>(p.seg, p.nseg, tile);
         const Seg sg = p.seg[s];
-        const int64_t i0 = sg.begin + (tile - sg.tile0) * (int64_t)kThreads * kScalarPerThread + threadIdx.x;
-#pragma unroll 4
-        for (int j = 0; j < kScalarPerThread; ++j) {
-            const int64_t i = i0 + (int64_t)j * kThreads;
-            if (i < sg.end) fused_scalar<E, OUT>(p, sg.c, i);
+        const int c = sg.c;
+        const int64_t t_in_seg = tile - sg.tile0;
+        int64_t ab, ae;
+        unaligned_interior(sg.begin, sg.end, V, &ab, &ae);
+        const int64_t first = ab + t_in_seg * (B / esz);
+        const int64_t left = (ae - first) * esz;
+        const int bytes = left <= 0 ? 0 : (int)(left < B ? left : B);
+
+        if (bytes > 0) {
+            if (threadIdx.x == 0) {
+                uint32_t total = 0;
+                for (int k = 0; k < n; ++k) {
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(p.rows[k]) + (uintptr_t)first * esz;
+                    const int d = (int)(a & 15);
+                    shift[k] = d;
+                    total += (uint32_t)((d + bytes + 15) & ~15);
+                }
+                asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_addr(bar)));
+                asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_addr(bar)), "r"(total)
+                             : "memory");
+                for (int k = 0; k < n; ++k) {
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(p.rows[k]) + (uintptr_t)first * esz;
+                    const int d = shift[k];
+                    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                                 :: "r"(smem_addr(smem + (size_t)k * slot)), "l"(a - d), "r"((d + bytes + 15) & ~15),
+                                    "r"(smem_addr(bar)) : "memory");
+                }
+            }
+            __syncthreads();
+            const bool ok = mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
+            if (__syncthreads_or(!ok)) {
+                if (threadIdx.x == 0) {
+                    atomicOr(&g_ra_device_error, 1u);
+                    mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
+                }
+                __syncthreads();
+                return;
+            }
+            const int ne = bytes / esz;
+            for (int j = threadIdx.x; j < ne; j += kThreads) {
+                auto staged = [&](int k) -> float {
+                    const T v = *reinterpret_cast<const T *>(smem + (size_t)k * slot + shift[k] + j * esz);
+                    if constexpr (esz == 4) return v; else return bf16_bits_to_f32(v);
+                };
+                float acc = staged(c);
+                int r = c;
+                for (int k = 1; k < n; ++k) {
+                    r = r + 1 == n ? 0 : r + 1;
+                    acc = __fadd_rn(staged(r), acc);
+                    if constexpr (OUT == kOutAllWire) acc = round_bf16(acc);
+                }
+                const float avg = div_n(acc, n);
+                const int64_t i = first + j;
+                if constexpr (OUT == kOutOne) {
+                    store_scalar_all<E>(&p.aux[c], 1, i, avg);
+                } else {
+                    const float held = store_scalar_all<E>(p.rows, n, i, avg);
+                    if constexpr (OUT == kOutAllSgd) p.w[i] = __fsub_rn(p.w[i], __fmul_rn(p.lr, held));
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" :: "r"(smem_addr(bar)) : "memory");
+            __syncthreads();
         }
+        // the margins and anything shorter than them: scalar path
+        if (t_in_seg == 0)
+            for (int64_t i = sg.begin + threadIdx.x; i < ab; i += kThreads) fused_scalar<E, OUT>(p, c, i);
+        const bool last = (s + 1 < p.nseg ? p.seg[s + 1].tile0 : p.ntiles) == tile + 1;
+        if (last)
+            for (int64_t i = (ae > ab ? ae : ab) + threadIdx.x; i < sg.end; i += kThreads) fused_scalar<E, OUT>(p, c, i);
     }
 }
 
