@@ -73,7 +73,7 @@ ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, con
     L.vector = vector;
     L.mis = mis;
     std::vector<Seg> tab(segs, segs + nseg);
-    L.tile_bytes = fused_tile_bytes(n, L.out == kOutOne);
+    L.tile_bytes = fused_tile_bytes(n, L.out == kOutOne, vector);
     const int64_t ntiles = vector ? fused_tma_assign_tiles(tab.data(), nseg, dtype, mis, L.tile_bytes)
                                   : fused_unaligned_assign_tiles(tab.data(), nseg, dtype, L.tile_bytes);
     L.seg = tab.data();

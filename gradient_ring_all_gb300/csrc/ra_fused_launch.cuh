@@ -49,7 +49,7 @@ static cudaError_t fused_unaligned_launch_one(const FusedLaunch &L, int64_t ntil
     TmaFusedParams<MAXSEG> tp;
     fill_params<E, OUT, MAXSEG>(tp.f, L, ntiles);
     tp.tile_bytes = L.tile_bytes;
-    const size_t smem = unaligned_smem_bytes(L.n, L.tile_bytes);
+    const size_t smem = unaligned_smem_bytes(L.n, L.tile_bytes, OUT, (int)sizeof(typename E::T));
     if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;
     // One tile per block.  The block scheduler hands out blocks in index
     // order, so the tiles in flight form one contiguous address window that

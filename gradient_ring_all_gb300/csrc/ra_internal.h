@@ -86,8 +86,14 @@ constexpr int64_t kTmaStageBytesOneOut = 65536;
 #ifndef RA_TMA_MIN_TILE_BYTES
 #define RA_TMA_MIN_TILE_BYTES 2048
 #endif
-inline int fused_tile_bytes(int n, bool one_destination) {
-    const int64_t budget = one_destination ? kTmaStageBytesOneOut : RA_TMA_STAGE_BYTES;
+// Rows without a common 16-byte boundary (the unaligned kernel) hold their
+// tile longer -- the mean leaves by scalar stores -- and want more bytes in
+// flight per block.
+#ifndef RA_UNALIGNED_STAGE_BYTES
+#define RA_UNALIGNED_STAGE_BYTES 32768
+#endif
+inline int fused_tile_bytes(int n, bool one_destination, bool vector) {
+    const int64_t budget = one_destination ? kTmaStageBytesOneOut : vector ? RA_TMA_STAGE_BYTES : RA_UNALIGNED_STAGE_BYTES;
     int b = 16384;
     while (b > RA_TMA_MIN_TILE_BYTES && (int64_t)b * n > budget) b >>= 1;
     return b;
@@ -106,9 +112,11 @@ __host__ __device__ inline void unaligned_interior(int64_t b, int64_t e, int V, 
     if (*ae < *ab) *ab = *ae = b;
 }
 // shared memory of the unaligned kernel: a slot of B + 16 bytes per row
-// (room for the widening), the mbarrier, and the per-row byte offsets
-inline size_t unaligned_smem_bytes(int n, int tile_bytes) {
-    return (size_t)n * (tile_bytes + 16) + 16 + (size_t)n * sizeof(int);
+// (room for the widening), a weight slot for SGD, the mbarrier, and the
+// per-row byte offsets
+inline size_t unaligned_smem_bytes(int n, int tile_bytes, int out, int esz) {
+    return (size_t)n * ((size_t)tile_bytes + 16) + (out == kOutAllSgd ? (size_t)(tile_bytes / esz) * 4 + 16 : 0) + 16 +
+           (size_t)(n + 1) * sizeof(int);
 }
 int64_t fused_unaligned_assign_tiles(Seg *seg, int nseg, int dtype, int tile_bytes);
 

@@ -374,27 +374,57 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
     }
 }
 
-// TMA kernel for rows that disagree modulo 16 bytes.  A bulk copy needs a
-// 16-byte-aligned source, so for each row thread 0 copies the aligned span
-// that covers the tile -- from the tile's first byte rounded down to the
-// end rounded up -- and the row's elements start d_k bytes into its staging
-// slot.  Threads read the staged values with scalar shared-memory loads,
-// fold them in ring order, and store the mean with scalar stores that are
-// coalesced across the warp.  Tiles keep 16 bytes away from both ends of
-// their segment (those elements take the scalar path), so the widened
-// copies never leave the segment's own bytes.
+// TMA kernel for rows that disagree modulo 16 bytes.  A bulk copy needs
+// 16-byte-aligned global addresses, and here every row sits at its own byte
+// offset d_k from that boundary.
+//   load:  for each row thread 0 copies the tile widened to 16-byte
+//          boundaries (first byte rounded down, end rounded up) into a slot
+//          of B + 16 bytes; the row's elements start d_k bytes into the slot.
+//   fold:  each thread takes J elements of the tile and walks the rows in
+//          ring order, reading every row at its own offset, so the per-row
+//          work (offset, address) is shared by J elements.
+//   store: the mean leaves by scalar stores, coalesced across the warp, as
+//          soon as it is known.  (Writing it back into shared memory first
+//          and storing whole 16-byte granules -- by bulk copies or by
+//          16-byte thread stores -- measured slower on GB300.)
+// The SGD weights are one more widened bulk copy in and, for their whole
+// granules, a bulk copy out.  Tiles keep 16 bytes away from both ends of
+// their segment (those elements take the scalar path), so the widened copies
+// never leave the segment's own bytes.
+template <class T>
+__device__ __forceinline__ float ld_staged(const unsigned char *p) {
+    if constexpr (sizeof(T) == 4) return *reinterpret_cast<const float *>(p);
+    else return bf16_bits_to_f32(*reinterpret_cast<const unsigned short *>(p));
+}
+template <class T>
+__device__ __forceinline__ void put_elem(void *p, T v) {
+    if constexpr (sizeof(T) == 4) __stcs(reinterpret_cast<float *>(p), v);
+    else __stcs(reinterpret_cast<unsigned short *>(p), v);
+}
+
+// Elements per thread per pass of the unaligned kernel, measured on GB300
+// with packed rows: 2 for the all-reduce (bf16 N=16: 6.47 TB/s, against 5.82
+// with 1 and 5.87 with 4; binary32 within 1 %), 4 for the reduce-scatter
+// (7.35 against 7.11 TB/s with 2).
+template <int OUT>
+constexpr int unaligned_per_thread() { return OUT == kOutOne ? 4 : 2; }
+
 template <class E, int OUT, int MAXSEG>
 __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __grid_constant__ TmaFusedParams<MAXSEG> tp) {
     using T = typename E::T;
     constexpr int V = E::kVec;
     constexpr int esz = (int)sizeof(T);
+    constexpr int J = unaligned_per_thread<OUT>();
     const FusedParams<MAXSEG> &p = tp.f;
     const int n = p.n;
-    const int B = tp.tile_bytes;          // bytes of each row per tile
-    const int slot = B + 16;              // staging slot per row: room for the widening
+    const int B = tp.tile_bytes;  // bytes of each row per tile
+    const int slot = B + 16;      // room for the widening
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)n * slot);
-    int *shift = reinterpret_cast<int *>(smem + (size_t)n * slot + 16);  // d_k: where row k's tile starts in its slot
+    // n row slots | weight slot (SGD) | mbarrier | offsets
+    unsigned char *wslot = smem + (size_t)n * slot;
+    const int wslot_bytes = OUT == kOutAllSgd ? (B / esz) * 4 + 16 : 0;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(wslot + wslot_bytes);
+    int *shift = reinterpret_cast<int *>(wslot + wslot_bytes + 16);  // d_k of row k; shift[n]: the weights'
 
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<MAXSEG>(p.seg, p.nseg, tile);
@@ -406,31 +436,43 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
         const int64_t first = ab + t_in_seg * (B / esz);
         const int64_t left = (ae - first) * esz;
         const int bytes = left <= 0 ? 0 : (int)(left < B ? left : B);
+        const int ne = bytes / esz;
 
         if (bytes > 0) {
             if (threadIdx.x == 0) {
                 uint32_t total = 0;
                 for (int k = 0; k < n; ++k) {
-                    const uintptr_t a = reinterpret_cast<uintptr_t>(p.rows[k]) + (uintptr_t)first * esz;
-                    const int d = (int)(a & 15);
+                    const int d = (int)((reinterpret_cast<uintptr_t>(p.rows[k]) + (uintptr_t)first * esz) & 15);
                     shift[k] = d;
                     total += (uint32_t)((d + bytes + 15) & ~15);
+                }
+                if constexpr (OUT == kOutAllSgd) {
+                    shift[n] = (int)((reinterpret_cast<uintptr_t>(p.w + first)) & 15);
+                    total += (uint32_t)((shift[n] + ne * 4 + 15) & ~15);
                 }
                 asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_addr(bar)));
                 asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
                 asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_addr(bar)), "r"(total)
                              : "memory");
                 for (int k = 0; k < n; ++k) {
-                    const uintptr_t a = reinterpret_cast<uintptr_t>(p.rows[k]) + (uintptr_t)first * esz;
                     const int d = shift[k];
+                    const char *src = reinterpret_cast<const char *>(p.rows[k]) + first * esz - d;
                     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                                 :: "r"(smem_addr(smem + (size_t)k * slot)), "l"(a - d), "r"((d + bytes + 15) & ~15),
+                                 :: "r"(smem_addr(smem + (size_t)k * slot)), "l"(src), "r"((d + bytes + 15) & ~15),
                                     "r"(smem_addr(bar)) : "memory");
+                }
+                if constexpr (OUT == kOutAllSgd) {
+                    const int d = shift[n];
+                    const char *src = reinterpret_cast<const char *>(p.w + first) - d;
+                    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                                 :: "r"(smem_addr(wslot)), "l"(src), "r"((d + ne * 4 + 15) & ~15), "r"(smem_addr(bar))
+                                 : "memory");
                 }
             }
             __syncthreads();
             const bool ok = mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
             if (__syncthreads_or(!ok)) {
+                // the copies never landed: record it, let them finish (bounded), leave
                 if (threadIdx.x == 0) {
                     atomicOr(&g_ra_device_error, 1u);
                     mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
@@ -438,30 +480,90 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
                 __syncthreads();
                 return;
             }
-            const int ne = bytes / esz;
-            for (int j = threadIdx.x; j < ne; j += kThreads) {
-                auto staged = [&](int k) -> float {
-                    const T v = *reinterpret_cast<const T *>(smem + (size_t)k * slot + shift[k] + j * esz);
-                    if constexpr (esz == 4) return v; else return bf16_bits_to_f32(v);
-                };
-                float acc = staged(c);
+            for (int j0 = threadIdx.x; j0 < ne; j0 += J * kThreads) {
+                float acc[J];
+                {
+                    const unsigned char *b = smem + (size_t)c * slot + shift[c];
+#pragma unroll
+                    for (int u = 0; u < J; ++u) {
+                        const int j = j0 + u * kThreads;
+                        acc[u] = j < ne ? ld_staged<T>(b + j * esz) : 0.f;
+                    }
+                }
                 int r = c;
                 for (int k = 1; k < n; ++k) {
                     r = r + 1 == n ? 0 : r + 1;
-                    acc = __fadd_rn(staged(r), acc);
-                    if constexpr (OUT == kOutAllWire) acc = round_bf16(acc);
+                    const unsigned char *b = smem + (size_t)r * slot + shift[r];
+#pragma unroll
+                    for (int u = 0; u < J; ++u) {
+                        const int j = j0 + u * kThreads;
+                        if (j < ne) {
+                            acc[u] = __fadd_rn(ld_staged<T>(b + j * esz), acc[u]);
+                            if constexpr (OUT == kOutAllWire) acc[u] = round_bf16(acc[u]);
+                        }
+                    }
                 }
-                const float avg = div_n(acc, n);
-                const int64_t i = first + j;
+                T v[J];
+                float held[J];
+#pragma unroll
+                for (int u = 0; u < J; ++u) {
+                    const float avg = div_n(acc[u], n);
+                    if constexpr (esz == 4) {
+                        v[u] = avg;
+                        held[u] = avg;
+                    } else {
+                        v[u] = (T)f32_to_bf16_bits(avg);
+                        held[u] = bf16_bits_to_f32(v[u]);
+                    }
+                }
                 if constexpr (OUT == kOutOne) {
-                    store_scalar_all<E>(&p.aux[c], 1, i, avg);
+                    char *base = reinterpret_cast<char *>(p.aux[c]) + first * esz;
+#pragma unroll
+                    for (int u = 0; u < J; ++u)
+                        if (j0 + u * kThreads < ne) put_elem<T>(base + (j0 + u * kThreads) * esz, v[u]);
                 } else {
-                    const float held = store_scalar_all<E>(p.rows, n, i, avg);
-                    if constexpr (OUT == kOutAllSgd) p.w[i] = __fsub_rn(p.w[i], __fmul_rn(p.lr, held));
+                    for (int k = 0; k < n; ++k) {
+                        char *base = reinterpret_cast<char *>(p.rows[k]) + first * esz;
+#pragma unroll
+                        for (int u = 0; u < J; ++u)
+                            if (j0 + u * kThreads < ne) put_elem<T>(base + (j0 + u * kThreads) * esz, v[u]);
+                    }
+                    if constexpr (OUT == kOutAllSgd) {
+                        // whole granules of the weights go back by bulk copy, the
+                        // partial ones at the tile's ends element by element
+                        const int d = shift[n], lo = (d + 15) & ~15, hi = (d + ne * 4) & ~15;
+#pragma unroll
+                        for (int u = 0; u < J; ++u) {
+                            const int j = j0 + u * kThreads;
+                            if (j < ne) {
+                                const int pos = d + j * 4;
+                                float *wp = reinterpret_cast<float *>(wslot + pos);
+                                const float nw = __fsub_rn(*wp, __fmul_rn(p.lr, held[u]));
+                                if (pos >= lo && pos < hi) *wp = nw;
+                                else __stcs(p.w + first + j, nw);
+                            }
+                        }
+                    }
                 }
             }
+            if constexpr (OUT == kOutAllSgd) {
+                // generic-proxy writes of the new weights -> visible to the bulk copy
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
             __syncthreads();
-            if (threadIdx.x == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" :: "r"(smem_addr(bar)) : "memory");
+            if (threadIdx.x == 0) {
+                if constexpr (OUT == kOutAllSgd) {
+                    const int d = shift[n], lo = (d + 15) & ~15, hi = (d + ne * 4) & ~15;
+                    if (hi > lo)
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                     :: "l"(reinterpret_cast<char *>(p.w + first) - d + lo), "r"(smem_addr(wslot + lo)),
+                                        "r"(hi - lo) : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    // the staged weights must stay valid until the copy has read them
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                }
+                asm volatile("mbarrier.inval.shared::cta.b64 [%0];" :: "r"(smem_addr(bar)) : "memory");
+            }
             __syncthreads();
         }
         // the margins and anything shorter than them: scalar path
