@@ -432,12 +432,18 @@ def run_profile_call(args):
     g = torch.Generator(device="cuda")
     g.manual_seed(wl.seed)
     rows = []
-    for _ in range(n):
-        r = torch.empty(p, dtype=torch.bfloat16 if bf16 else torch.float32, device="cuda")
+    dt = torch.bfloat16 if bf16 else torch.float32
+    if args.layout == "strided":
+        # rows back to back with a stride of p + 1 elements: they disagree
+        # modulo 16 bytes, the case of the unaligned kernel
+        big = torch.empty(n * (p + 1), dtype=dt, device="cuda")
+        rows = [big[k * (p + 1):k * (p + 1) + p] for k in range(n)]
+    else:
+        rows = [torch.empty(p, dtype=dt, device="cuda") for _ in range(n)]
+    for r in rows:
         tmp = torch.randn(p, generator=g, device="cuda") * wl.scale
         r.copy_(tmp)
         del tmp
-        rows.append(r)
     stream = torch.cuda.current_stream()
     c = args.call
     if c == "allreduce":
@@ -471,7 +477,7 @@ def run_profile_call(args):
     _, ms = timed_region(lambda k: step(), args.steps, None, _CudaEventTimer(stream))
     ms /= args.steps
     nbytes = call_bytes(c, n, p, esz)
-    print(json.dumps({"profile_run": True, "workload": args.workload, "call": c, "workers": n,
+    print(json.dumps({"profile_run": True, "workload": args.workload, "call": c, "layout": args.layout, "workers": n,
                       "elements_per_worker": p, "ms_per_step": ms, "algorithmic_bytes": nbytes,
                       "gbs": nbytes / (ms / 1e3) / 1e9}), flush=True)
     return 0
@@ -555,6 +561,8 @@ def main(argv=None):
                     help="profiling only (with --call): the synthetic workload to run")
     ap.add_argument("--call", choices=CALLS, default=None,
                     help="profiling only: time one entry point on --workload, device loop only")
+    ap.add_argument("--layout", choices=["separate", "strided"], default="separate",
+                    help="--call: one allocation per worker, or rows back to back with stride P+1 elements")
     ap.add_argument("--overlap", action="store_true",
                     help="experiment: bucketed all-reduce overlapped with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=8192, help="--overlap: tokens per backward step")
