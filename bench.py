@@ -393,14 +393,14 @@ def run_ours(args):
     return 0
 
 
-CALLS = ("allreduce", "staged", "sgd", "buckets", "reduce_scatter", "all_gather", "single_reducer", "bf16_wire",
-         "host")
+CALLS = ("allreduce", "staged", "sgd", "buckets", "buckets_each", "reduce_scatter", "all_gather", "single_reducer",
+         "bf16_wire", "host")
 
 
 def call_bytes(call: str, n: int, p: int, esz: int) -> int:
     """Algorithmic bytes one call moves: every byte its design must read or
     write once (the staged ring's own schedule for `staged`)."""
-    if call in ("allreduce", "buckets", "single_reducer", "bf16_wire", "host"):
+    if call in ("allreduce", "buckets", "buckets_each", "single_reducer", "bf16_wire", "host"):
         return 2 * n * p * esz
     if call == "sgd":
         return 2 * n * p * esz + 2 * p * 4
@@ -458,6 +458,12 @@ def run_profile_call(args):
     elif c == "buckets":
         plan = ra.ra_bucket_plan(wl.tensors, esz, wl.bucket_cap_bytes or 25 * 1024 * 1024)
         step = lambda: ra.ra_allreduce_avg_buckets(rows, plan, stream)
+    elif c == "buckets_each":  # one call, and so one launch, per bucket
+        plan = ra.ra_bucket_plan(wl.tensors, esz, wl.bucket_cap_bytes or 25 * 1024 * 1024)
+
+        def step():
+            for b in plan:
+                ra.ra_allreduce_avg_buckets(rows, [b], stream)
     elif c == "reduce_scatter":
         step = lambda: ra.ra_reduce_scatter_avg(rows, None, stream)
     elif c == "all_gather":

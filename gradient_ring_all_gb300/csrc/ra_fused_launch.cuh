@@ -58,8 +58,7 @@ static cudaError_t fused_unaligned_launch_one(const FusedLaunch &L, int64_t ntil
     // 6.28 TB/s at N=8, P=300M f32).  The kernel's tile loop only matters
     // past 2^31-1 tiles.
     const int64_t grid = ntiles < kMaxGrid ? ntiles : kMaxGrid;
-    kern<<<(unsigned)grid, kThreadsPerBlock, smem, s>>>(tp);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, kThreadsPerBlock, smem, s, tp);
 }
 
 template <class E>
@@ -93,8 +92,7 @@ static cudaError_t fused_tma_launch_one(const FusedLaunch &L, int64_t ntiles, cu
     if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;
     // one tile per block (see fused_unaligned_launch_one)
     const int64_t grid = ntiles < kMaxGrid ? ntiles : kMaxGrid;
-    kern<<<(unsigned)grid, kThreadsPerBlock, smem, s>>>(tp);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, kThreadsPerBlock, smem, s, tp);
 }
 
 // vector path: the TMA kernel, the fold unrolled for the common worker counts

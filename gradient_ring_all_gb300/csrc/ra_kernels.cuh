@@ -230,6 +230,41 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Programmatic dependent launch.  The fused kernels are launched with
+// programmatic stream serialisation, so the next kernel on the stream may be
+// launched while this one drains its last wave.  Every block first allows
+// that (the next grid starts only once all blocks of this one have started),
+// then waits until the previous grid on the stream has completed and its
+// writes are visible, before touching global memory.  Without the launch
+// attribute both instructions do nothing.
+#ifndef RA_PDL
+#define RA_PDL 1
+#endif
+__device__ __forceinline__ void pdl_enter() {
+#if RA_PDL
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
+// host side: launch with programmatic stream serialisation (every kernel of
+// this library calls pdl_enter before its first global access)
+template <class K, class... P>
+static cudaError_t launch_pdl(K kern, int64_t grid, int block, size_t smem, cudaStream_t s, const P &...params) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = RA_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, params...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: copies of one tile take microseconds
 
 template <int MAXSEG>
@@ -283,6 +318,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
     float *wt = reinterpret_cast<float *>(outb + B);  // SGD: the weights of the tile, (B / esz) * 4 bytes
     const int wbytes_max = OUT == kOutAllSgd ? (B / esz) * 4 : 0;
     uint64_t *bar = reinterpret_cast<uint64_t *>(outb + B + wbytes_max);
+    pdl_enter();
 
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<MAXSEG>(p.seg, p.nseg, tile);
@@ -425,6 +461,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
     const int wslot_bytes = OUT == kOutAllSgd ? (B / esz) * 4 + 16 : 0;
     uint64_t *bar = reinterpret_cast<uint64_t *>(wslot + wslot_bytes);
     int *shift = reinterpret_cast<int *>(wslot + wslot_bytes + 16);  // d_k of row k; shift[n]: the weights'
+    pdl_enter();
 
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<MAXSEG>(p.seg, p.nseg, tile);
@@ -697,6 +734,7 @@ __device__ __forceinline__ void staged_vector(const StagedParams &p, int c, int6
 template <class E, bool VECTOR>
 __global__ void __launch_bounds__(kThreads) staged_step_kernel(const __grid_constant__ StagedParams p) {
     constexpr int V = E::kVec;
+    pdl_enter();
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<RA_MAX_N>(p.seg, p.nseg, tile);
         const Seg sg = p.seg[s];
@@ -751,6 +789,7 @@ __device__ __forceinline__ void gather_scalar(const GatherParams &p, int c, int6
 // scalar all-gather, for rows (or shards) that share no 16-byte boundary
 template <class E>
 __global__ void __launch_bounds__(kThreads) all_gather_scalar_kernel(const __grid_constant__ GatherParams p) {
+    pdl_enter();
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<RA_MAX_N>(p.seg, p.nseg, tile);
         const Seg sg = p.seg[s];
@@ -773,6 +812,7 @@ __global__ void __launch_bounds__(32) all_gather_tma_kernel(const __grid_constan
     const int B = tile_bytes;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + B);
+    pdl_enter();
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int s = find_seg<RA_MAX_N>(p.seg, p.nseg, tile);
         const Seg sg = p.seg[s];

@@ -20,8 +20,7 @@ static cudaError_t staged_launch_one(const StagedLaunch &L, int op, int t, cudaS
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
     // one tile per block, as for the fused kernel
     const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
-    staged_step_kernel<E, VEC><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(staged_step_kernel<E, VEC>, grid, kThreadsPerBlock, 0, s, p);
 }
 
 cudaError_t launch_staged_step(const StagedLaunch &L, int op, int t, cudaStream_t s) {
@@ -46,8 +45,7 @@ static cudaError_t gather_scalar_launch(const GatherLaunch &L, cudaStream_t s) {
     p.ntiles = L.ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
     const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
-    all_gather_scalar_kernel<E><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(all_gather_scalar_kernel<E>, grid, kThreadsPerBlock, 0, s, p);
 }
 
 template <class E>
@@ -77,8 +75,7 @@ static cudaError_t gather_tma_launch(const GatherLaunch &L, cudaStream_t s) {
         }
     }
     const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
-    all_gather_tma_kernel<E><<<(unsigned)grid, 32, smem, s>>>(p, kGatherTileBytes);
-    return cudaGetLastError();
+    return launch_pdl(all_gather_tma_kernel<E>, grid, 32, smem, s, p, kGatherTileBytes);
 }
 
 cudaError_t launch_all_gather(const GatherLaunch &L, cudaStream_t s) {

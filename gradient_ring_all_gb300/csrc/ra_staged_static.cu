@@ -59,8 +59,7 @@ cudaError_t setup_device(int dev, DeviceSetup *out) {
 template <class E, bool VEC>
 cudaError_t launch_step(const StagedParams &p, cudaStream_t s) {
     const int64_t grid = p.ntiles < kMaxGrid ? p.ntiles : kMaxGrid;
-    staged_step_kernel<E, VEC><<<(unsigned)grid, kThreadsPerBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(staged_step_kernel<E, VEC>, grid, kThreadsPerBlock, 0, s, p);
 }
 
 cudaError_t launch_step_any(const StagedParams &p, int dtype, bool vec, cudaStream_t s) {
