@@ -121,22 +121,25 @@ def _dtype_code(t) -> int:
 
 def _rows(tensors):
     """(pointer array, n, p, dtype code, device) for a list of worker tensors."""
-    tensors = list(tensors)
+    if not isinstance(tensors, (list, tuple)):
+        tensors = list(tensors)
     if not tensors:
         raise ValueError("need at least one worker buffer")
     n = len(tensors)
     t0 = tensors[0]
     dt = _dtype_code(t0)
-    p = t0.numel()
-    for t in tensors:
-        if not t.is_cuda:
-            raise ValueError("worker buffers must be CUDA tensors")
-        if t.dtype != t0.dtype or t.numel() != p or t.device != t0.device:
+    dtype, p, dev = t0.dtype, t0.numel(), t0.get_device()
+    ptrs = [0] * n
+    for k, t in enumerate(tensors):
+        # one pass, integer device ids: this runs on every call
+        if t.get_device() != dev or dev < 0:
+            raise ValueError("worker buffers must be CUDA tensors on one device")
+        if t.dtype != dtype or t.numel() != p:
             raise ValueError("worker buffers must share dtype, length and device")
         if not t.is_contiguous():
             raise ValueError("worker buffers must be contiguous")
-    arr = (ctypes.c_void_p * n)(*[t.data_ptr() for t in tensors])
-    return arr, n, p, dt, t0.device
+        ptrs[k] = t.data_ptr()
+    return (ctypes.c_void_p * n)(*ptrs), n, p, dt, t0.device
 
 
 def _stream(stream, device):
