@@ -105,8 +105,8 @@ def walk(n, esz, rows, out, segs, w, aux, budget, margin=True):
                         pos = d + 4 * j
                         if not lo <= pos < hi:
                             wr("w", a + 4 * j, a + 4 * j + 4)
-            margin = (list(range(b, ab)) if t == 0 else []) + (list(range(max(ae, ab), e)) if t == nt - 1 else [])
-            for i in margin:
+            edges = (list(range(b, ab)) if t == 0 else []) + (list(range(max(ae, ab), e)) if t == nt - 1 else [])
+            for i in edges:
                 if out == "one":
                     wr("aux", aux[c] + i * esz, aux[c] + (i + 1) * esz)
                 else:
