@@ -1,12 +1,46 @@
 // ra_api.cu -- the C ABI (include/ring_allreduce.h): argument checks, the
 // cutting of a request into ring-chunk segments, and kernel dispatch.
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 #include <utility>
 #include <vector>
 
 #include "ra_internal.h"
 
 namespace ra {
+
+// The error word every bounded wait reports to (one per device, since a
+// __device__ variable exists once in each device's copy of the module).
+static __device__ unsigned int g_device_error_word = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned int *> g_error_word_addr[kMaxDevices];
+std::mutex g_error_word_mu;
+}  // namespace
+
+cudaError_t device_error_word(unsigned int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned int *a = g_error_word_addr[dev].load(std::memory_order_acquire);
+    if (a == nullptr) {
+        std::lock_guard<std::mutex> lk(g_error_word_mu);
+        a = g_error_word_addr[dev].load(std::memory_order_acquire);
+        if (a == nullptr) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_device_error_word);
+            if (e != cudaSuccess) return e;
+            a = static_cast<unsigned int *>(p);
+            g_error_word_addr[dev].store(a, std::memory_order_release);
+        }
+    }
+    *out = a;
+    return cudaSuccess;
+}
+
 namespace {
 
 thread_local int g_last_cuda_error = 0;
@@ -79,7 +113,9 @@ ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, con
     L.seg = tab.data();
     L.nseg = nseg;
     if (ntiles == 0) return RA_OK;
-    cudaError_t e = dtype == RA_F32 ? launch_fused_f32(L, ntiles, s) : launch_fused_bf16(L, ntiles, s);
+    cudaError_t e = device_error_word(&L.err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = dtype == RA_F32 ? launch_fused_f32(L, ntiles, s) : launch_fused_bf16(L, ntiles, s);
     return e == cudaSuccess ? RA_OK : cuda_fail(e);
 }
 
@@ -442,7 +478,9 @@ ra_status ra_all_gather(void *const *bufs, int n, int64_t p, int dtype, void *co
                         : staged_assign_tiles(segs.data(), (int)segs.size(), dtype, false, mis);
     L.seg = segs.data();
     L.nseg = (int)segs.size();
-    cudaError_t e = launch_all_gather(L, static_cast<cudaStream_t>(stream));
+    cudaError_t e = device_error_word(&L.err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_all_gather(L, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RA_OK : cuda_fail(e);
 }
 
@@ -476,16 +514,19 @@ ra_status ra_allreduce_avg_single_reducer(void *const *bufs, int n, int64_t p, i
 }
 
 ra_status ra_check_device_errors(void) {
-    unsigned int flags = 0;
-    cudaError_t e = collect_device_error_f32(&flags);
-    if (e == cudaSuccess) e = collect_device_error_bf16(&flags);
+    unsigned int flags = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&flags, g_device_error_word, sizeof(flags));
+    if (e == cudaSuccess && flags) e = cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero));
     if (e != cudaSuccess) return cuda_fail(e);
     return flags ? RA_ERR_TIMEOUT : RA_OK;
 }
 
 ra_status ra_selftest_wait_timeout(int timeout_us, void *stream) {
     if (timeout_us < 1 || timeout_us > 10000000) return RA_ERR_INVALID_ARG;
-    cudaError_t e = launch_wait_timeout_selftest((uint64_t)timeout_us * 1000ull, static_cast<cudaStream_t>(stream));
+    unsigned int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e == cudaSuccess)
+        e = launch_wait_timeout_selftest((uint64_t)timeout_us * 1000ull, err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RA_OK : cuda_fail(e);
 }
 

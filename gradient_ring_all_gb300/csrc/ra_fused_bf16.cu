@@ -6,5 +6,4 @@ namespace ra {
 cudaError_t launch_fused_bf16(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     return fused_launch_dtype<BF16>(L, ntiles, s);
 }
-cudaError_t collect_device_error_bf16(unsigned int *flags) { return collect_device_error<BF16>(flags); }
 }  // namespace ra

@@ -5,12 +5,11 @@ namespace ra {
 cudaError_t launch_fused_f32(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     return fused_launch_dtype<F32>(L, ntiles, s);
 }
-cudaError_t collect_device_error_f32(unsigned int *flags) { return collect_device_error<F32>(flags); }
 
 // A wait that cannot end: an mbarrier expecting 16 bytes that no copy will
 // deliver.  The bounded wait gives up after limit_ns, records the error and
 // returns -- the library's self-test of the timeout path.
-__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, unsigned int *err) {
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_addr(&bar)));
@@ -18,11 +17,11 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 16;" :: "r"(smem_addr(&bar)) : "memory");
     }
     __syncthreads();
-    if (!mbar_wait_bounded(smem_addr(&bar), 0, limit_ns) && threadIdx.x == 0) atomicOr(&g_ra_device_error, 1u);
+    if (!mbar_wait_bounded(smem_addr(&bar), 0, limit_ns) && threadIdx.x == 0) atomicOr(err, 1u);
 }
 
-cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t s) {
-    wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned int *err, cudaStream_t s) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, err);
     return cudaGetLastError();
 }
 }  // namespace ra

@@ -49,6 +49,7 @@ static cudaError_t fused_unaligned_launch_one(const FusedLaunch &L, int64_t ntil
     TmaFusedParams<MAXSEG> tp;
     fill_params<E, OUT, MAXSEG>(tp.f, L, ntiles);
     tp.tile_bytes = L.tile_bytes;
+    tp.err = L.err;
     const size_t smem = unaligned_smem_bytes(L.n, L.tile_bytes, OUT, (int)sizeof(typename E::T));
     if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;
     // One tile per block.  The block scheduler hands out blocks in index
@@ -87,6 +88,7 @@ static cudaError_t fused_tma_launch_one(const FusedLaunch &L, int64_t ntiles, cu
     TmaFusedParams<MAXSEG> tp;
     fill_params<E, OUT, MAXSEG>(tp.f, L, ntiles);
     tp.tile_bytes = L.tile_bytes;
+    tp.err = L.err;
     const int esz = (int)sizeof(typename E::T);
     const size_t smem = (size_t)L.n * L.tile_bytes + L.tile_bytes + (OUT == kOutAllSgd ? L.tile_bytes / esz * 4 : 0) + 16;
     if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;
@@ -131,15 +133,6 @@ static cudaError_t fused_tma_dispatch(const FusedLaunch &L, int64_t ntiles, cuda
             return fused_tma_dispatch_nt<E, 0>(L, ntiles, s);
         default: return fused_tma_dispatch_nt<E, 0>(L, ntiles, s);
     }
-}
-
-template <class E>
-static cudaError_t collect_device_error(unsigned int *flags) {
-    unsigned int v = 0, zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&v, g_ra_device_error, sizeof(v));
-    if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_ra_device_error, &zero, sizeof(zero));
-    *flags |= v;
-    return e;
 }
 
 template <class E>

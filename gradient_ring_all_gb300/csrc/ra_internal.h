@@ -67,6 +67,7 @@ struct FusedLaunch {
     const Seg *seg;  // host table, tile0 filled by the launcher
     int nseg;
     int tile_bytes;  // vector path: bytes per row per tile
+    unsigned int *err;  // the device's error word (device_error_word)
 };
 
 // Vector path of the fused kernel: bytes of each row one block stages in
@@ -120,10 +121,13 @@ inline size_t unaligned_smem_bytes(int n, int tile_bytes, int out, int esz) {
 }
 int64_t fused_unaligned_assign_tiles(Seg *seg, int nseg, int dtype, int tile_bytes);
 
-// collect and clear the device error flags of the fused-kernel translation units
-cudaError_t collect_device_error_f32(unsigned int *flags);
-cudaError_t collect_device_error_bf16(unsigned int *flags);
-cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t s);
+// The current device's error word: one unsigned int in device memory that
+// every kernel with a bounded wait ORs bit 0 into when the wait gives up.
+// It is a file-scope __device__ variable of ra_api.cu; its address is looked
+// up once per device (cudaGetSymbolAddress) and passed to the kernels in
+// their parameters, so all translation units report to the same word.
+cudaError_t device_error_word(unsigned int **out);
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned int *err, cudaStream_t s);
 
 // fill seg[].tile0 and return the tile count of the staged kernel
 int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis);
@@ -156,6 +160,7 @@ struct GatherLaunch {
     const Seg *seg;
     int nseg;
     int64_t ntiles;  // scalar kernel: staged-size tiles; vector: kGatherTileBytes tiles
+    unsigned int *err;  // the device's error word (device_error_word)
 };
 cudaError_t launch_all_gather(const GatherLaunch &L, cudaStream_t s);
 

@@ -206,10 +206,6 @@ constexpr int kThreads = kThreadsPerBlock;
 // copies (shared -> global).  The copy engine holds the bytes in flight, so
 // the fold needs no per-n register arrays and one kernel serves every n.
 
-// Device-side error flag, one per translation unit (bit 0: a bounded wait
-// gave up); the host collects and clears it (ra_check_device_errors).
-static __device__ unsigned int g_ra_device_error = 0;
-
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -270,6 +266,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: copies of one tile tak
 template <int MAXSEG>
 struct TmaFusedParams {
     FusedParams<MAXSEG> f;  // rows, aux, w, lr, n, nseg, mis, ntiles, seg
+    unsigned int *err;      // the device's error word: bit 0 = a bounded wait gave up
     int tile_bytes;         // bytes per row per tile (multiple of 16)
 };
 
@@ -352,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
             if (__syncthreads_or(!ok)) {
                 // the copies never landed: record it, let them finish (bounded), leave
                 if (threadIdx.x == 0) {
-                    atomicOr(&g_ra_device_error, 1u);
+                    atomicOr(tp.err, 1u);
                     mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
                 }
                 __syncthreads();
@@ -511,7 +508,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
             if (__syncthreads_or(!ok)) {
                 // the copies never landed: record it, let them finish (bounded), leave
                 if (threadIdx.x == 0) {
-                    atomicOr(&g_ra_device_error, 1u);
+                    atomicOr(tp.err, 1u);
                     mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
                 }
                 __syncthreads();
@@ -773,6 +770,7 @@ struct GatherParams {
     int nseg;
     int mis;
     int skip_owner;       // 1: the source is the owner's own array, which is not rewritten
+    unsigned int *err;    // the device's error word: bit 0 = a bounded wait gave up
     int64_t ntiles;
     Seg seg[RA_MAX_N];
 };
@@ -838,7 +836,7 @@ __global__ void __launch_bounds__(32) all_gather_tma_kernel(const __grid_constan
         // the whole warp leaves together if the copy never landed
         if (__shfl_sync(0xffffffffu, fail, 0)) {
             if (threadIdx.x == 0) {
-                atomicOr(&g_ra_device_error, 1u);
+                atomicOr(p.err, 1u);
                 mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
             }
             return;

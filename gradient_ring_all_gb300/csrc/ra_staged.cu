@@ -42,6 +42,7 @@ static cudaError_t gather_scalar_launch(const GatherLaunch &L, cudaStream_t s) {
     p.nseg = L.nseg;
     p.mis = L.mis;
     p.skip_owner = L.skip_owner ? 1 : 0;
+    p.err = L.err;
     p.ntiles = L.ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
     const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
@@ -60,6 +61,7 @@ static cudaError_t gather_tma_launch(const GatherLaunch &L, cudaStream_t s) {
     p.nseg = L.nseg;
     p.mis = L.mis;
     p.skip_owner = L.skip_owner ? 1 : 0;
+    p.err = L.err;
     p.ntiles = L.ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
     const size_t smem = (size_t)kGatherTileBytes + 16;

@@ -36,17 +36,25 @@
  *     kernel variant in a process, which loads its module; with CUDA's lazy
  *     module loading (the default) that load may synchronise the context,
  *     so warm a call up once (or set CUDA_MODULE_LOADING=EAGER) before
- *     relying on overlap.
+ *     relying on overlap.  The first launching call on a device also looks
+ *     up the address of the device's error word (cudaGetSymbolAddress);
+ *     like that first launch, it belongs before any stream capture.
  *   - Arguments are checked before anything is queued; a non-OK status
  *     means nothing was launched.  RA_ERR_CUDA reports a failed launch or
  *     device query; ra_last_cuda_error() returns its cudaError_t value.
  *   - n == 1 or p == 0: nothing to reduce, RA_OK without a launch (x / 1 is
  *     exact).  The SGD call still updates w when n == 1.
- *   - Pointers whose addresses agree modulo 16 bytes take the 128-bit
- *     vector path; any other element-aligned pointers take a scalar path
- *     with the same results.
+ *   - Pointers whose addresses agree modulo 16 bytes take the vector path
+ *     (TMA bulk copies of whole 16-byte granules); any other element-aligned
+ *     pointers take the unaligned path (bulk copies widened to 16-byte
+ *     boundaries inside each row's own range) with the same results.
+ *   - Kernels are launched with programmatic dependent launch: the next
+ *     launch on the stream may start while the current one drains, and
+ *     every kernel waits for the previous grid on the stream to finish
+ *     before touching memory, so stream order holds as usual.
  *   - Every function is thread-safe; the library keeps no state besides
- *     the per-device address of its one built-in scratch array.
+ *     the per-device addresses of its built-in scratch array and of its
+ *     error word.
  */
 #ifndef RING_ALLREDUCE_H
 #define RING_ALLREDUCE_H
@@ -317,11 +325,12 @@ ra_status ra_reducer_destroy(ra_reducer *r);
 
 /*
  * ra_check_device_errors -- whether a kernel of this library on the current
- * device gave up a bounded wait since the last check.  The fused kernels
- * wait for their bulk copies (global -> shared memory) on an mbarrier; each
- * wait is limited to 2 s (the copies of one tile take microseconds), after
- * which the kernel records the failure, skips its stores and returns, so the
- * context stays usable.  Returns RA_ERR_TIMEOUT if such a record exists (the
+ * device gave up a bounded wait since the last check.  The TMA kernels
+ * (fused all-reduce in all its variants, all-gather) wait for their bulk
+ * copies (global -> shared memory) on an mbarrier; each wait is limited to
+ * 2 s (the copies of one tile take microseconds), after which the kernel
+ * records the failure in the device's error word, skips its stores and
+ * returns, so the context stays usable.  Returns RA_ERR_TIMEOUT if such a record exists (the
  * results of the calls in flight at the time are then invalid), RA_OK
  * otherwise, and clears the record.  Reads device memory synchronously:
  * call it after the streams in question have finished.
