@@ -115,16 +115,19 @@ static cudaError_t fused_tma_dispatch_nt(const FusedLaunch &L, int64_t ntiles, c
     }
 }
 
-// Which worker counts get the unrolled fold was measured on GB300: it wins at
-// n = 4 (7.05 vs 6.92 TB/s), ties at 8, edges ahead for binary32 at 32, and
-// loses for bf16 at 16 (6.89 vs 7.05 TB/s), where the runtime loop is kept.
+// Which worker counts get the unrolled fold was measured on GB300: binary32
+// gains at n = 4 (7.05 vs 6.92 TB/s) and 8 (7.08 vs 6.94), and edges ahead at
+// 32; bf16 keeps the runtime loop at 8 (7.06 vs 6.70 TB/s unrolled) and 16
+// (7.05 vs 6.89), and is even at 2 and 4.
 template <class E>
 static cudaError_t fused_tma_dispatch(const FusedLaunch &L, int64_t ntiles, cudaStream_t s) {
     constexpr bool wide = sizeof(typename E::T) == 4;
     switch (L.n) {
         case 2: return fused_tma_dispatch_nt<E, 2>(L, ntiles, s);
         case 4: return fused_tma_dispatch_nt<E, 4>(L, ntiles, s);
-        case 8: return fused_tma_dispatch_nt<E, 8>(L, ntiles, s);
+        case 8:
+            if constexpr (wide) return fused_tma_dispatch_nt<E, 8>(L, ntiles, s);
+            return fused_tma_dispatch_nt<E, 0>(L, ntiles, s);
         case 16:
             if constexpr (wide) return fused_tma_dispatch_nt<E, 16>(L, ntiles, s);
             return fused_tma_dispatch_nt<E, 0>(L, ntiles, s);

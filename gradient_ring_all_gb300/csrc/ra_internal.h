@@ -70,34 +70,41 @@ struct FusedLaunch {
     unsigned int *err;  // the device's error word (device_error_word)
 };
 
-// Vector path of the fused kernel: bytes of each row one block stages in
-// shared memory, so that the n staged rows take about RA_TMA_STAGE_BYTES (at
-// least 2 KB per row).  Measured on GB300 against 64 KB per block: equal at
-// N=8 (7.10 TB/s), +0.4 % at N=4 (bucketed), -0.2 % for bf16 at N=16, and
-// +4 % on rows in host memory, where more, smaller tiles hide the longer
-// latency.
-// The reduce-scatter writes one row per tile instead of n, so its single
-// bulk store gets a larger tile (64 KB staged: 7.39 vs 7.22 TB/s at N=8).
+// Tile size of the fused kernels: bytes of each row one block stages in
+// shared memory.  The n staged rows take about a budget per block --
+// RA_TMA_STAGE_BYTES for the vector path, more for the unaligned kernel,
+// which holds its tile longer, and 64 KB for the reduce-scatter, which writes
+// one row per tile instead of n -- with the tile a multiple of 16 bytes
+// between 2 KB and 16 KB, and at most RA_TMA_MAX_STAGE_BYTES staged per
+// block (so that several blocks share an SM even at n = 64).
+// Measured on GB300, all-reduce at 9.6 GB per call:
+//  - 16 KB budget against 64 KB: equal at n=8 (7.10 TB/s), +0.4 % at n=4,
+//    -0.2 % for bf16 at n=16, +4 % on rows in host memory;
+//  - tiles sized to the budget, not rounded down to a power of two: n=3
+//    6.86 (was 6.32), n=5 6.98 (5.75), n=7 6.88 (6.54) TB/s in binary32;
+//  - 1 KB minimum instead of 2 KB: n=32 6.01 against 6.97 TB/s;
+//  - 64 KB cap per block: n=64 6.88 against 5.07 TB/s (one 128 KB block per
+//    SM); a 96 KB cap gave 6.87 (binary32) and 6.66 (bf16, against 6.79).
 #ifndef RA_TMA_STAGE_BYTES
 #define RA_TMA_STAGE_BYTES 16384
 #endif
 constexpr int64_t kTmaStageBytesOneOut = 65536;
-// Smallest tile per row: 1 KB tiles measured worse everywhere on HBM
-// (N=8 6.19, N=32 5.95 TB/s), and only 1 % better on host memory.
-#ifndef RA_TMA_MIN_TILE_BYTES
-#define RA_TMA_MIN_TILE_BYTES 2048
-#endif
-// Rows without a common 16-byte boundary (the unaligned kernel) hold their
-// tile longer -- the mean leaves by scalar stores -- and want more bytes in
-// flight per block.
 #ifndef RA_UNALIGNED_STAGE_BYTES
 #define RA_UNALIGNED_STAGE_BYTES 32768
 #endif
+#ifndef RA_TMA_MIN_TILE_BYTES
+#define RA_TMA_MIN_TILE_BYTES 2048
+#endif
+#ifndef RA_TMA_MAX_STAGE_BYTES
+#define RA_TMA_MAX_STAGE_BYTES 65536
+#endif
 inline int fused_tile_bytes(int n, bool one_destination, bool vector) {
     const int64_t budget = one_destination ? kTmaStageBytesOneOut : vector ? RA_TMA_STAGE_BYTES : RA_UNALIGNED_STAGE_BYTES;
-    int b = 16384;
-    while (b > RA_TMA_MIN_TILE_BYTES && (int64_t)b * n > budget) b >>= 1;
-    return b;
+    int64_t b = (budget / n) & ~(int64_t)15;
+    if (b < RA_TMA_MIN_TILE_BYTES) b = RA_TMA_MIN_TILE_BYTES;
+    if (b > 16384) b = 16384;
+    if (b * n > RA_TMA_MAX_STAGE_BYTES) b = (RA_TMA_MAX_STAGE_BYTES / n) & ~(int64_t)15;
+    return (int)b;
 }
 constexpr int kMaxDynamicSmem = 227 * 1024;
 

@@ -14,9 +14,10 @@ and what the caller's buffers need:
 - the bytes of one barrier's copies stay under the mbarrier's 2^20 limit;
 - every destination byte is written exactly once.
 
-The constants mirror the library's tile sizing (ra_internal.h): 2 KB minimum
-and 16 KB maximum per row, 32 KB staged per block, 64 KB for the
-reduce-scatter.
+The tile rule mirrors the library's (ra_internal.h): the staging budget
+divided by n, rounded down to 16 bytes, kept between 2 KB and 16 KB per row,
+and cut so that no block stages more than 64 KB; the budget is 32 KB per
+block for this kernel and 64 KB for the reduce-scatter.
 """
 from __future__ import annotations
 
@@ -28,14 +29,21 @@ import oracle
 
 UNALIGNED_STAGE = 32768
 ONE_DEST_STAGE = 65536
+MAX_STAGE = 65536
 
 
 def tile_bytes(n, one_destination, budget=UNALIGNED_STAGE):
     budget = ONE_DEST_STAGE if one_destination else budget
-    b = 16384
-    while b > 2048 and b * n > budget:
-        b >>= 1
+    b = min(16384, max(2048, (budget // n) & ~15))
+    if b * n > MAX_STAGE:
+        b = (MAX_STAGE // n) & ~15
     return b
+
+
+def test_tile_rule_examples():
+    # odd worker counts get tiles that fill the budget; n = 64 is cut to 64 KB per block
+    assert [tile_bytes(n, False, 16384) for n in (2, 3, 5, 8, 16, 33, 64)] == [8192, 5456, 3264, 2048, 2048, 1984, 1024]
+    assert [tile_bytes(n, True) for n in (2, 8, 64)] == [16384, 8192, 1024]
 
 
 def rup(x):
