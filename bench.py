@@ -426,7 +426,7 @@ def run_profile_call(args):
     import gradient_ring_all_gb300 as ra
     import synth
     wl = synth.WORKLOADS[args.workload]
-    n, p = wl.n, (args.elements or wl.p)
+    n, p = (args.workers or wl.n), (args.elements or wl.p)
     bf16 = wl.dtype == "bf16"
     esz = 2 if bf16 else 4
     g = torch.Generator(device="cuda")
@@ -567,6 +567,8 @@ def main(argv=None):
                     help="profiling only (with --call): the synthetic workload to run")
     ap.add_argument("--call", choices=CALLS, default=None,
                     help="profiling only: time one entry point on --workload, device loop only")
+    ap.add_argument("--workers", type=int, default=0,
+                    help="--call: worker count instead of the workload's (with --elements for the length)")
     ap.add_argument("--layout", choices=["separate", "strided"], default="separate",
                     help="--call: one allocation per worker, or rows back to back with stride P+1 elements")
     ap.add_argument("--overlap", action="store_true",
