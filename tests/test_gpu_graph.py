@@ -72,3 +72,88 @@ def test_graph_replay_matches_eager_and_oracle():
     torch.cuda.synchronize()
     for r, e in zip(rows, eager):
         assert torch.equal(r, e)
+
+
+CALLS = ["avg", "staged", "staged_static", "sgd", "reduce_scatter", "all_gather", "single_reducer", "bf16_wire",
+         "buckets"]
+
+
+def _run(call, rows, w, ws, plan):
+    if call == "avg":
+        ra.ra_allreduce_avg(rows)
+    elif call == "staged":
+        ra.ra_allreduce_avg_staged(rows, ws)
+    elif call == "staged_static":
+        ra.ra_allreduce_avg_staged_static(rows)
+    elif call == "sgd":
+        ra.ra_allreduce_sgd(rows, w, 0.1)
+    elif call == "reduce_scatter":
+        ra.ra_reduce_scatter_avg(rows)
+    elif call == "all_gather":
+        ra.ra_all_gather(rows)
+    elif call == "single_reducer":
+        ra.ra_allreduce_avg_single_reducer(rows)
+    elif call == "bf16_wire":
+        ra.ra_allreduce_avg_bf16_wire(rows)
+    else:
+        ra.ra_allreduce_avg_buckets(rows, plan)
+
+
+@pytest.mark.parametrize("layout", ["separate", "strided"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("call", CALLS)
+def test_every_call_replays_like_eager(call, dtype, layout):
+    # every entry point, captured after an eager warm-up, replayed twice from
+    # fresh inputs; the staged ring captures its whole chain of launches
+    if call == "bf16_wire" and dtype == "f32":
+        pytest.skip("the bf16-wire ring is defined for bf16 gradients")
+    n, p = 5, 300_007
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    src = [(torch.randn(p, device="cuda", generator=gen) * 1e-2).to(tdt) for _ in range(n)]
+    w0 = torch.randn(p, device="cuda", generator=gen) * 0.05
+
+    def buffers():
+        if layout == "strided":  # rows that share no 16-byte boundary
+            big = torch.empty(n * (p + 1), dtype=tdt, device="cuda")
+            return [big[k * (p + 1):k * (p + 1) + p] for k in range(n)]
+        return [torch.empty(p, dtype=tdt, device="cuda") for _ in range(n)]
+
+    plan = ra.ra_bucket_plan([p // 3, p // 3, p - 2 * (p // 3)], 4 if dtype == "f32" else 2, 1 << 18)
+    ws = torch.empty(max(1, ra.ra_staged_workspace_bytes(n, p, 0 if dtype == "f32" else 1)), dtype=torch.uint8,
+                     device="cuda")
+    # eager reference
+    eager, we = buffers(), w0.clone()
+    for r, x in zip(eager, src):
+        r.copy_(x)
+    _run(call, eager, we, ws, plan)
+    # captured
+    rows, w = buffers(), torch.empty_like(w0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for r, x in zip(rows, src):
+            r.copy_(x)
+        w.copy_(w0)
+        _run(call, rows, w, ws, plan)  # warm-up on the capture stream
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for r, x in zip(rows, src):
+            r.copy_(x)
+        w.copy_(w0)
+        _run(call, rows, w, ws, plan)
+    for _ in range(2):
+        for r in rows:
+            r.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    bits = (lambda t: t.view(torch.int16)) if dtype == "bf16" else (lambda t: t.view(torch.int32))
+    if call == "reduce_scatter":  # only each worker's own chunk is defined
+        for k in range(n):
+            b, e = oracle.chunk_range(p, n, oracle.owned_chunk(n, k))
+            assert torch.equal(bits(rows[k][b:e]), bits(eager[k][b:e]))
+    else:
+        for r, e in zip(rows, eager):
+            assert torch.equal(bits(r), bits(e))
+    if call == "sgd":
+        assert torch.equal(w.view(torch.int32), we.view(torch.int32))
