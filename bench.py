@@ -209,6 +209,15 @@ def _oracle_step(wl, rows, w, plan):
         oracle.sgd_update_f32(w, rows[0], wl.sgd_lr)
 
 
+def _config(wl, n, p, ws):
+    """The `config` object of the bench line (both arms print the same one)."""
+    esz = 4 if wl.dtype == "f32" else 2
+    return {"workload": wl.name, "workers": n, "elements_per_worker": p,
+            "distribution": "N(0, %g), seed %d, worker n = generator stream n" % (wl.scale, wl.seed),
+            "bytes_per_step": 2 * n * p * esz, "parallelism": "replicas" if ws > 1 else "single GPU",
+            "l2": "inputs of %.1f GB per GPU, larger than the 129 MB L2; no flush" % (n * p * esz / 1e9)}
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -245,13 +254,13 @@ def run_reference(args):
     total = sum(times)
     nbytes = 2 * wl.n * p * esz + (2 * p * 4 if w is not None else 0)
     value = nbytes * args.steps / total / 1e9
-    sample = "N=%d workers x P=%d %s elements of %s per step, in place" % (wl.n, p, wl.dtype, wl.name)
+    sample = ("N=%d workers x P=%d %s elements of %s per step (a bounded sample of its P=%d), in place, "
+              "one core" % (wl.n, p, wl.dtype, wl.name, wl.p))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
-        "data": "synthetic", "config": {"workload": wl.name, "workers": wl.n, "elements_per_worker": p,
-                                        "note": "CPU oracle on a bounded sample of the workload"},
+        "data": "synthetic", "config": _config(wl, wl.n, wl.p, ws),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -359,10 +368,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "workers": n, "elements_per_worker": p,
-                   "distribution": "N(0, %g), seed %d, worker n = generator stream n" % (wl.scale, wl.seed),
-                   "bytes_per_step": nbytes, "parallelism": "replicas" if ws > 1 else "single GPU",
-                   "l2": "inputs of %.1f GB per GPU, larger than the 129 MB L2; no flush" % (n * p * 4 / 1e9)},
+        "config": _config(wl, n, p, ws),
         "pct_of_measured_hbm": 100.0 * value / ws / peak,
         "pct_of_nominal_hbm": 100.0 * value / ws / NOMINAL_HBM_GBS,
         "elements_per_s": n * p * ws / (ms_per_step / 1e3),
