@@ -21,11 +21,11 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -67,12 +67,9 @@ class _ClockSampler:
 
     def start(self):
         try:
-            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
-            os.close(fd)
-            self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
                                           "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=self.out, stderr=subprocess.DEVNULL)
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
@@ -82,17 +79,15 @@ class _ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
-            self.proc.wait(timeout=5)
+            out, _ = self.proc.communicate(timeout=5)
         except Exception:
             self.proc.kill()
-        self.out.close()
+            out, _ = self.proc.communicate()
         rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
-        os.unlink(self.path)
+        for line in (out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -102,13 +97,21 @@ class _ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
 
 
-def _source_hash() -> str:
+def _code_only(src: str) -> str:
+    """C/CUDA source without comments and with whitespace collapsed, so that
+    the hash changes with the code and not with its comments."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def _source_hash(csrc_dir: str | None = None) -> str:
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "gradient_ring_all_gb300", "csrc")
+    d = csrc_dir or os.path.join(ROOT, "gradient_ring_all_gb300", "csrc")
     for f in sorted(os.listdir(d)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(d, f), encoding="utf-8") as fh:
+                h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

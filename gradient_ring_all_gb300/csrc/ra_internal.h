@@ -66,7 +66,7 @@ struct FusedLaunch {
     int mis;
     const Seg *seg;  // host table, tile0 filled by the launcher
     int nseg;
-    int tile_bytes;  // vector path: bytes per row per tile
+    int tile_bytes;  // bytes of each row per tile (fused_tile_bytes)
     unsigned int *err;  // the device's error word (device_error_word)
 };
 
