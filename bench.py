@@ -47,6 +47,20 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# A replica that dies or stops between steps must not hold the others (and
+# their GPUs) for the default 30-minute collective timeout: their next
+# barrier fails after this many seconds instead.
+PG_TIMEOUT_S = float(os.environ.get("RA_BENCH_PG_TIMEOUT_S", "600"))
+
+
+def init_replicas():
+    """The replicas' gloo group, with the bounded timeout above."""
+    import datetime
+    import torch.distributed as dist
+    dist.init_process_group("gloo", timeout=datetime.timedelta(seconds=PG_TIMEOUT_S))
+    return dist
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -281,8 +295,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dist = None
     if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo")
+        dist = init_replicas()
     from gradient_ring_all_gb300 import build
     build.build()
     import gradient_ring_all_gb300 as ra

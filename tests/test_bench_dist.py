@@ -86,3 +86,47 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _failing_rank_main(rank, world, port, mode, q):
+    # rank 1 fails between steps: it exits, or stops answering; rank 0 must
+    # get an error from its next barrier instead of waiting for it forever
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      RA_BENCH_PG_TIMEOUT_S="5")
+    sys.path.insert(0, ROOT)
+    import bench
+    dist = bench.init_replicas()
+    bench.timed_region(lambda k: None, 1, dist, _WallTimer())  # one good step together
+    if rank == 1:
+        if mode == "exit":
+            os._exit(3)
+        time.sleep(40)  # stops answering
+        os._exit(0)
+    t0 = time.perf_counter()
+    try:
+        bench.timed_region(lambda k: None, 1, dist, _WallTimer())
+        q.put((rank, "no error", time.perf_counter() - t0))
+    except Exception as e:  # the failure surfaces as an exception
+        q.put((rank, type(e).__name__, time.perf_counter() - t0))
+
+
+@pytest.mark.parametrize("mode", ["exit", "hang"])
+def test_a_failed_replica_surfaces_as_an_error_not_a_hang(mode):
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_failing_rank_main, args=(r, 2, port, mode, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    try:
+        rank, outcome, waited = q.get(timeout=120)
+    finally:
+        for p in procs:
+            p.join(timeout=10)
+            if p.is_alive():
+                p.kill()  # our own child (the rank that stopped answering)
+                p.join()
+    assert rank == 0
+    assert outcome != "no error"
+    assert waited < 30, waited  # the 5 s timeout, not the default 30 minutes
