@@ -126,3 +126,34 @@ def test_student_t3_1g_n16_bf16_rows_without_common_alignment():
     del rows, big
     gc.collect()
     torch.cuda.empty_cache()
+
+
+def test_more_than_2_pow_31_elements_rows_without_common_alignment():
+    # N=2 rows of 2^31 + 1001 fp32 elements at stride P+1 (8.6 GB each):
+    # element indices past 2^31 in the widened-copy kernel must not wrap
+    n, p = 2, (1 << 31) + 1001
+    big = torch.empty(n * (p + 1), dtype=torch.float32, device="cuda")
+    rows = [big[k * (p + 1):k * (p + 1) + p] for k in range(n)]
+    assert len({r.data_ptr() % 16 for r in rows}) > 1
+    piece = 1 << 27
+    host = torch.empty(piece, dtype=torch.float32).pin_memory()
+    for k, r in enumerate(rows):
+        for s in range(0, p, piece):
+            c = min(piece, p - s)
+            synth.fill_normal_f32(host.data_ptr(), 78, k, 1.0, s, c)
+            r[s:s + c].copy_(host[:c])
+    ra.ra_allreduce_avg(rows)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(6)
+    idx = np.unique(np.concatenate([rng.integers(0, p, 500), np.arange(p - 40, p),
+                                    np.arange((1 << 31) - 20, (1 << 31) + 20),
+                                    np.arange(p // 2 - 10, p // 2 + 10)])).astype(np.int64)
+    vals = [synth.normal_f32_at(78, k, 1.0, idx) for k in range(n)]
+    want = np.array([oracle.ring_avg_point_f32(np.array([vals[0][j], vals[1][j]], np.float32), p, int(idx[j]))
+                     for j in range(idx.size)], np.float32)
+    for g in gather(rows, idx):
+        np.testing.assert_array_equal(g.view(np.uint32), want.view(np.uint32))
+    assert torch.equal(rows[0].view(torch.int32), rows[1].view(torch.int32))
+    del rows, big
+    gc.collect()
+    torch.cuda.empty_cache()
