@@ -9,6 +9,11 @@ unless ``stream`` (a cudaStream_t as int, or a torch.cuda.Stream) is given.
 
 There is no CPU fallback: if the shared library is missing this module
 raises on first use.
+
+With GRADIENT_RING_ALL_CHECKED=1 in the environment the bounds-checked build
+(libgradient_ring_all_checked.so, ``build.build(checked=True)``) is loaded
+instead: its kernels verify every global range they touch and report a
+violation as RA_ERR_BOUNDS through ra_check_device_errors.  The tests use it.
 """
 from __future__ import annotations
 
@@ -20,7 +25,8 @@ __all__ = [
     "ra_allreduce_avg", "ra_allreduce_sgd", "ra_allreduce_avg_staged", "ra_staged_workspace_bytes",
     "ra_bucket_plan", "ra_allreduce_avg_buckets", "ra_allreduce_avg_host", "ra_allreduce_avg_staged_static",
     "RA_STAGED_STATIC_MAX_P", "RA_HOST_AUTO", "RA_HOST_DIRECT", "RA_HOST_STAGED", "ra_reduce_scatter_avg",
-    "ra_all_gather", "ra_allreduce_avg_bf16_wire", "ra_allreduce_avg_single_reducer", "Reducer", "ra_check_device_errors", "ra_selftest_wait_timeout", "ra_chunk_range", "ra_status_str", "ra_last_cuda_error",
+    "ra_all_gather", "ra_allreduce_avg_bf16_wire", "ra_allreduce_avg_single_reducer", "Reducer", "ra_check_device_errors", "ra_selftest_wait_timeout", "ra_selftest_bounds_check", "ra_chunk_range", "ra_status_str",
+    "ra_last_cuda_error", "RA_OK", "RA_ERR_TIMEOUT", "RA_ERR_BOUNDS", "CHECKED",
 ]
 
 RA_F32 = 0
@@ -28,9 +34,11 @@ RA_BF16 = 1
 RA_MAX_N = 64
 RA_STAGED_STATIC_MAX_P = 4194304
 RA_HOST_AUTO, RA_HOST_DIRECT, RA_HOST_STAGED = 0, 1, 2
+RA_OK, RA_ERR_TIMEOUT, RA_ERR_BOUNDS = 0, 5, 6
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "lib", "libgradient_ring_all.so")
+CHECKED = os.environ.get("GRADIENT_RING_ALL_CHECKED") == "1"
+_LIB_PATH = os.path.join(_HERE, "lib", "libgradient_ring_all_checked.so" if CHECKED else "libgradient_ring_all.so")
 _lib = None
 
 
@@ -63,8 +71,8 @@ def load():
     if _lib is not None:
         return _lib
     if not os.path.exists(_LIB_PATH):
-        raise RuntimeError("libgradient_ring_all.so is not built (%s); run "
-                           "`python -m gradient_ring_all_gb300.build` first" % _LIB_PATH)
+        raise RuntimeError("%s is not built; run `python -m gradient_ring_all_gb300.build%s` first"
+                           % (_LIB_PATH, " --checked" if CHECKED else ""))
     lib = ctypes.CDLL(_LIB_PATH)
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     pvp = ctypes.POINTER(ctypes.c_void_p)
@@ -90,6 +98,7 @@ def load():
     lib.ra_reducer_destroy.argtypes = [vp]
     lib.ra_check_device_errors.argtypes = []
     lib.ra_selftest_wait_timeout.argtypes = [i32, vp]
+    lib.ra_selftest_bounds_check.argtypes = [pvp, i32, i64, i32, vp]
     lib.ra_chunk_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.ra_chunk_range.restype = None
     lib.ra_status_str.argtypes = [i32]
@@ -100,7 +109,7 @@ def load():
                "ra_reduce_scatter_avg", "ra_all_gather", "ra_allreduce_avg_bf16_wire",
                "ra_allreduce_avg_single_reducer", "ra_reducer_create", "ra_reducer_buckets",
                "ra_reducer_mark_ready", "ra_reducer_finish", "ra_reducer_destroy", "ra_check_device_errors",
-               "ra_selftest_wait_timeout", "ra_last_cuda_error"):
+               "ra_selftest_wait_timeout", "ra_selftest_bounds_check", "ra_last_cuda_error"):
         getattr(lib, nm).restype = i32
     _lib = lib
     return lib
@@ -359,9 +368,19 @@ class Reducer:
 
 
 def ra_check_device_errors() -> int:
-    """Status of the kernels' bounded waits on the current device since the
-    last check: 0 (RA_OK) or 5 (RA_ERR_TIMEOUT); clears the record."""
+    """What the kernels on the current device recorded since the last check:
+    0 (RA_OK), 5 (RA_ERR_TIMEOUT: a bounded wait gave up) or, in the
+    bounds-checked build, 6 (RA_ERR_BOUNDS); clears the record."""
     return int(load().ra_check_device_errors())
+
+
+def ra_selftest_bounds_check(tensors, stream=None) -> None:
+    """Bounds-checked build: run the fused all-reduce while telling the kernel
+    the rows are one element shorter than they are, so that the check must
+    report RA_ERR_BOUNDS (rows' contents afterwards unspecified).  The
+    product build raises RaError(RA_ERR_UNSUPPORTED)."""
+    arr, n, p, dt, dev = _rows(tensors)
+    _check(load().ra_selftest_bounds_check(arr, n, p, dt, _stream(stream, dev)), "ra_selftest_bounds_check")
 
 
 def ra_selftest_wait_timeout(timeout_us: int, stream=None) -> None:

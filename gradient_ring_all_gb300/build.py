@@ -1,10 +1,14 @@
 """Build the CUDA library in-tree for sm_103a (GB300).
 
-    python -m gradient_ring_all_gb300.build [--force] [--verbose-ptxas]
+    python -m gradient_ring_all_gb300.build [--force] [--verbose-ptxas] [--checked]
 
 Compiles each csrc/*.cu into _build/*.o in parallel with nvcc and links
 lib/libgradient_ring_all.so against the shared CUDA runtime.  A stamp of the
-sources and flags skips the work when nothing changed.
+sources and flags skips the work when nothing changed.  --checked builds the
+bounds-checked library instead (RA_CHECKED=1: every kernel verifies each
+global range it touches and reports a violation through the error word),
+into _build_checked/ and lib/libgradient_ring_all_checked.so; the tests use
+it, the product does not.
 """
 from __future__ import annotations
 
@@ -21,6 +25,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libgradient_ring_all.so")
+LIB_CHECKED = os.path.join(LIBDIR, "libgradient_ring_all_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
@@ -56,21 +61,27 @@ def _stamp(extra) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool | None = None) -> str:
+    if checked is None:  # the library the binding will load
+        checked = os.environ.get("GRADIENT_RING_ALL_CHECKED") == "1"
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    stamp_file = os.path.join(BUILD, "stamp")
+    if checked:
+        extra.append("-DRA_CHECKED=1")
+    bdir = BUILD + "_checked" if checked else BUILD
+    lib = LIB_CHECKED if checked else LIB
+    stamp_file = os.path.join(bdir, "stamp")
     stamp = _stamp(extra)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_file):
+    if not force and os.path.exists(lib) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
-                return LIB
+                return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     cu, _ = _sources()
 
     def compile_one(f):
-        obj = os.path.join(BUILD, f[:-3] + ".o")
+        obj = os.path.join(bdir, f[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, f), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -82,18 +93,19 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if verbose_ptxas:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     libdir = _cuda_lib_dir(nvcc)
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
            "-Xlinker", "-rpath," + libdir]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="--verbose-ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="--verbose-ptxas" in sys.argv,
+                checked=True if "--checked" in sys.argv else None))

@@ -92,9 +92,10 @@ void ring_segments(int64_t off, int64_t count, int n, std::vector<Seg> *out) {
     }
 }
 
-ra_status run_fused(void *const *bufs, int n, int dtype, float *w, float lr, const Seg *segs, int nseg, bool vector,
-                    int mis, cudaStream_t s, void *const *aux = nullptr, bool bf16_wire = false) {
+ra_status run_fused(void *const *bufs, int n, int64_t p, int dtype, float *w, float lr, const Seg *segs, int nseg,
+                    bool vector, int mis, cudaStream_t s, void *const *aux = nullptr, bool bf16_wire = false) {
     FusedLaunch L;
+    L.p = p;
     for (int k = 0; k < n; ++k) {
         L.rows[k] = bufs[k];
         L.aux[k] = aux ? aux[k] : nullptr;
@@ -230,7 +231,7 @@ ra_status ra_allreduce_avg(void *const *bufs, int n, int64_t p, int dtype, void 
     ring_segments(0, p, n, &segs);
     int mis = 0;
     const bool vector = common_misalignment(bufs, n, dtype, &mis);
-    return run_fused(bufs, n, dtype, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
+    return run_fused(bufs, n, p, dtype, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
                      static_cast<cudaStream_t>(stream));
 }
 
@@ -254,7 +255,7 @@ ra_status ra_allreduce_sgd(void *const *bufs, int n, int64_t p, int dtype, float
     bool vector = common_misalignment(bufs, n, dtype, &mis);
     // the weights are read as float4 at the rows' vector boundaries
     if (vector && (int)((wa / 4) % 4) != mis % 4) vector = false;
-    return run_fused(bufs, n, dtype, w, lr, segs.data(), (int)segs.size(), vector, mis,
+    return run_fused(bufs, n, p, dtype, w, lr, segs.data(), (int)segs.size(), vector, mis,
                      static_cast<cudaStream_t>(stream));
 }
 
@@ -308,9 +309,17 @@ ra_status ra_allreduce_avg_staged(void *const *bufs, int n, int64_t p, int dtype
     // binary32 partial sums for bf16, placed so that msg + i is 16-byte
     // aligned exactly when the rows' element i starts a vector
     L.msg = nullptr;
+    L.msg_lo = L.msg_hi = nullptr;
     if (dtype == RA_BF16) {
         const uintptr_t base = (wsa + 15) & ~(uintptr_t)15;
         L.msg = reinterpret_cast<float *>(base + (uintptr_t)(L.vector ? 4 * (mis % 4) : 0));
+        L.msg_lo = reinterpret_cast<const char *>(wsa);
+        L.msg_hi = reinterpret_cast<const char *>(wsa + ws_bytes);
+    }
+    L.p = p;
+    {
+        cudaError_t e = device_error_word(&L.err);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     std::vector<Seg> segs;
     ring_segments(0, p, n, &segs);
@@ -383,7 +392,7 @@ ra_status ra_allreduce_avg_buckets(void *const *bufs, int n, int dtype, const ra
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (size_t k0 = 0; k0 < segs.size(); k0 += kSegLarge) {
         const int cnt = (int)std::min<size_t>(kSegLarge, segs.size() - k0);
-        st = run_fused(bufs, n, dtype, nullptr, 0.f, segs.data() + k0, cnt, vector, mis, s);
+        st = run_fused(bufs, n, extent, dtype, nullptr, 0.f, segs.data() + k0, cnt, vector, mis, s);
         if (st != RA_OK) return st;
     }
     return RA_OK;
@@ -455,7 +464,7 @@ ra_status ra_reduce_scatter_avg(void *const *bufs, int n, int64_t p, int dtype, 
     if (st != RA_OK) return st;
     std::vector<Seg> segs;
     ring_segments(0, p, n, &segs);
-    return run_fused(bufs, n, dtype, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
+    return run_fused(bufs, n, p, dtype, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
                      static_cast<cudaStream_t>(stream), base);
 }
 
@@ -470,6 +479,7 @@ ra_status ra_all_gather(void *const *bufs, int n, int64_t p, int dtype, void *co
     L.vector = common_misalignment(bufs, n, dtype, &mis);
     L.mis = mis;
     L.skip_owner = shards == nullptr;
+    L.p = p;
     st = shard_bases(bufs, n, p, dtype, shards, L.src, &L.vector, mis);
     if (st != RA_OK) return st;
     std::vector<Seg> segs;
@@ -491,7 +501,7 @@ ra_status ra_allreduce_avg_bf16_wire(void *const *bufs, int n, int64_t p, void *
     ring_segments(0, p, n, &segs);
     int mis = 0;
     const bool vector = common_misalignment(bufs, n, RA_BF16, &mis);
-    return run_fused(bufs, n, RA_BF16, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
+    return run_fused(bufs, n, p, RA_BF16, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
                      static_cast<cudaStream_t>(stream), nullptr, true);
 }
 
@@ -510,7 +520,7 @@ ra_status ra_allreduce_avg_single_reducer(void *const *bufs, int n, int64_t p, i
     const Seg seg{0, p, 0, 0, 0};
     int mis = 0;
     const bool vector = common_misalignment(bufs, n, dtype, &mis);
-    return run_fused(bufs, n, dtype, nullptr, 0.f, &seg, 1, vector, mis, static_cast<cudaStream_t>(stream));
+    return run_fused(bufs, n, p, dtype, nullptr, 0.f, &seg, 1, vector, mis, static_cast<cudaStream_t>(stream));
 }
 
 ra_status ra_check_device_errors(void) {
@@ -518,7 +528,21 @@ ra_status ra_check_device_errors(void) {
     cudaError_t e = cudaMemcpyFromSymbol(&flags, g_device_error_word, sizeof(flags));
     if (e == cudaSuccess && flags) e = cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero));
     if (e != cudaSuccess) return cuda_fail(e);
-    return flags ? RA_ERR_TIMEOUT : RA_OK;
+    return (flags & 2u) ? RA_ERR_BOUNDS : (flags ? RA_ERR_TIMEOUT : RA_OK);
+}
+
+ra_status ra_selftest_bounds_check(void *const *bufs, int n, int64_t p, int dtype, void *stream) {
+    ra_status st = check_rows(bufs, n, p, dtype);
+    if (st != RA_OK) return st;
+    if (n < 2 || p < 2) return RA_ERR_INVALID_ARG;
+    if (!RA_CHECKED) return RA_ERR_UNSUPPORTED;
+    // the ring's segments over all p elements, the kernel's bound one short
+    std::vector<Seg> segs;
+    ring_segments(0, p, n, &segs);
+    int mis = 0;
+    const bool vector = common_misalignment(bufs, n, dtype, &mis);
+    return run_fused(bufs, n, p - 1, dtype, nullptr, 0.f, segs.data(), (int)segs.size(), vector, mis,
+                     static_cast<cudaStream_t>(stream));
 }
 
 ra_status ra_selftest_wait_timeout(int timeout_us, void *stream) {
@@ -550,6 +574,7 @@ const char *ra_status_str(int status) {
         case RA_ERR_OVERLAP: return "RA_ERR_OVERLAP";
         case RA_ERR_CUDA: return "RA_ERR_CUDA";
         case RA_ERR_TIMEOUT: return "RA_ERR_TIMEOUT";
+        case RA_ERR_BOUNDS: return "RA_ERR_BOUNDS";
         default: return "RA_UNKNOWN_STATUS";
     }
 }

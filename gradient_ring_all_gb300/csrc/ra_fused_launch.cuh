@@ -17,10 +17,12 @@ static void fill_params(FusedParams<MAXSEG> &p, const FusedLaunch &L, int64_t nt
         p.aux[k] = L.aux[k];
     }
     p.w = L.w;
+    p.err = L.err;
     p.lr = L.lr;
     p.n = L.n;
     p.nseg = L.nseg;
     p.mis = L.mis;
+    p.p = L.p;
     p.ntiles = ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
 }
@@ -49,7 +51,6 @@ static cudaError_t fused_unaligned_launch_one(const FusedLaunch &L, int64_t ntil
     TmaFusedParams<MAXSEG> tp;
     fill_params<E, OUT, MAXSEG>(tp.f, L, ntiles);
     tp.tile_bytes = L.tile_bytes;
-    tp.err = L.err;
     const size_t smem = unaligned_smem_bytes(L.n, L.tile_bytes, OUT, (int)sizeof(typename E::T));
     if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;
     // One tile per block.  The block scheduler hands out blocks in index
@@ -88,7 +89,6 @@ static cudaError_t fused_tma_launch_one(const FusedLaunch &L, int64_t ntiles, cu
     TmaFusedParams<MAXSEG> tp;
     fill_params<E, OUT, MAXSEG>(tp.f, L, ntiles);
     tp.tile_bytes = L.tile_bytes;
-    tp.err = L.err;
     const int esz = (int)sizeof(typename E::T);
     const size_t smem = (size_t)L.n * L.tile_bytes + L.tile_bytes + (OUT == kOutAllSgd ? L.tile_bytes / esz * 4 : 0) + 16;
     if (smem > (size_t)kMaxDynamicSmem) return cudaErrorInvalidValue;

@@ -21,6 +21,11 @@ struct Seg {
 };
 static_assert(sizeof(Seg) == 32, "Seg layout");
 
+// RA_CHECKED=1 builds the bounds-checked library (see ra_kernels.cuh)
+#ifndef RA_CHECKED
+#define RA_CHECKED 0
+#endif
+
 constexpr int kThreadsPerBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;  // largest gridDim.x
 constexpr int kScalarPerThread = 4;  // elements per thread per tile, scalar staged and gather paths
@@ -68,6 +73,7 @@ struct FusedLaunch {
     int nseg;
     int tile_bytes;  // bytes of each row per tile (fused_tile_bytes)
     unsigned int *err;  // the device's error word (device_error_word)
+    int64_t p;          // elements per row: the rows are [rows[k], rows[k] + p)
 };
 
 // Tile size of the fused kernels: bytes of each row one block stages in
@@ -146,6 +152,9 @@ cudaError_t launch_fused_bf16(const FusedLaunch &L, int64_t ntiles, cudaStream_t
 struct StagedLaunch {
     void *rows[RA_MAX_N];
     float *msg;
+    const char *msg_lo, *msg_hi;  // the caller's workspace
+    unsigned int *err;            // the device's error word
+    int64_t p;                    // elements per row
     int n;
     int dtype;
     bool vector;
@@ -168,6 +177,7 @@ struct GatherLaunch {
     int nseg;
     int64_t ntiles;  // scalar kernel: staged-size tiles; vector: kGatherTileBytes tiles
     unsigned int *err;  // the device's error word (device_error_word)
+    int64_t p;          // elements per row
 };
 cudaError_t launch_all_gather(const GatherLaunch &L, cudaStream_t s);
 

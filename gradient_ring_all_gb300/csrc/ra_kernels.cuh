@@ -146,15 +146,40 @@ __device__ __forceinline__ int ring_idx(int c, int k, int n) {
 // binary32 value of the nearest bf16 (ties to even)
 __device__ __forceinline__ float round_bf16(float x) { return bf16_bits_to_f32(f32_to_bf16_bits(x)); }
 
+// The bounds-checked build (compiled with RA_CHECKED=1 into a separate
+// library for the tests): before each global access a kernel verifies that
+// the range lies inside the caller's buffer it belongs to -- a row
+// [rows[k], rows[k] + p), the weights [w, w + p), chunk c of a shard or of the
+// all-gather's source, the staged workspace -- and the bulk copies of a tile
+// also inside the tile's segment.  A violation sets bit 1 of the error word
+// and the access is skipped, so nothing outside the buffers is touched.  The
+// product build compiles every check away.
+constexpr bool kChecked = RA_CHECKED != 0;
+constexpr unsigned int kErrBounds = 2u;
+
+__device__ __forceinline__ bool span_in(const void *a, int64_t bytes, const void *lo, int64_t len) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), b = reinterpret_cast<uintptr_t>(lo);
+    return bytes >= 0 && len >= 0 && x >= b && x + (uintptr_t)bytes <= b + (uintptr_t)len;
+}
+// chunk c of a p-element array split for n workers (the first p mod n
+// chunks hold one extra element)
+__device__ __forceinline__ void chunk_span(int64_t p, int n, int c, int64_t *b, int64_t *e) {
+    const int64_t q = p / n, r = p % n;
+    *b = (int64_t)c * q + (c < r ? c : r);
+    *e = *b + q + (c < r ? 1 : 0);
+}
+
 template <int MAXSEG>
 struct FusedParams {
     void *rows[RA_MAX_N];  // worker arrays (device)
     void *aux[RA_MAX_N];   // kOutOne: element i of chunk c goes to aux[c] + i * element size
     float *w;              // SGD weights (device) or null
+    unsigned int *err;     // the device's error word: bit 0 = a bounded wait gave up
     float lr;
     int n;                 // workers
     int nseg;
     int mis;               // rows' common misalignment, in elements (< kVec); vector mode only
+    int64_t p;             // elements per row (the bounds the checked build verifies)
     int64_t ntiles;
     Seg seg[MAXSEG];
 };
@@ -179,6 +204,18 @@ __device__ __forceinline__ int find_seg(const Seg *seg, int nseg, int64_t tile) 
 // one element through the scalar path: ring-order fold from worker c
 template <class E, int OUT, int MAXSEG>
 __device__ __forceinline__ void fused_scalar(const FusedParams<MAXSEG> &p, int c, int64_t i) {
+    if constexpr (kChecked) {
+        bool ok = i >= 0 && i < p.p;
+        if constexpr (OUT == kOutOne) {
+            int64_t b, e;
+            chunk_span(p.p, p.n, c, &b, &e);
+            ok = ok && i >= b && i < e;
+        }
+        if (!ok) {
+            atomicOr(p.err, kErrBounds);
+            return;
+        }
+    }
     const int n = p.n;
     float acc = load_scalar<E>(p.rows[c], i);
     for (int k = 1; k < n; ++k) {
@@ -265,8 +302,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: copies of one tile tak
 
 template <int MAXSEG>
 struct TmaFusedParams {
-    FusedParams<MAXSEG> f;  // rows, aux, w, lr, n, nseg, mis, ntiles, seg
-    unsigned int *err;      // the device's error word: bit 0 = a bounded wait gave up
+    FusedParams<MAXSEG> f;  // rows, aux, w, err, lr, n, nseg, mis, p, ntiles, seg
     int tile_bytes;         // bytes per row per tile (multiple of 16)
 };
 
@@ -330,6 +366,26 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
         const int wbytes = OUT == kOutAllSgd ? (bytes / esz) * 4 : 0;
 
         if (bytes > 0) {
+            if constexpr (kChecked) {
+                // every copy of the tile inside its segment of its buffer
+                if (threadIdx.x == 0) {
+                    bool ok = sg.begin >= 0 && sg.end <= p.p && first >= sg.begin && first * esz + bytes <= sg.end * esz;
+                    for (int k = 0; k < n; ++k)
+                        ok = ok && span_in(reinterpret_cast<const char *>(p.rows[k]) + first * esz, bytes, p.rows[k],
+                                           p.p * esz);
+                    if constexpr (OUT == kOutAllSgd) ok = ok && span_in(p.w + first, wbytes, p.w, p.p * 4);
+                    if constexpr (OUT == kOutOne) {
+                        int64_t b, e;
+                        chunk_span(p.p, p.n, c, &b, &e);
+                        ok = ok && span_in(reinterpret_cast<const char *>(p.aux[c]) + first * esz, bytes,
+                                           reinterpret_cast<const char *>(p.aux[c]) + b * esz, (e - b) * esz);
+                    }
+                    if (!ok) atomicOr(p.err, kErrBounds);
+                    reinterpret_cast<int *>(bar + 1)[0] = ok ? 0 : 1;  // the spare half of the barrier's slot
+                }
+                __syncthreads();
+                if (reinterpret_cast<volatile int *>(bar + 1)[0]) return;
+            }
             if (threadIdx.x == 0) {
                 asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_addr(bar)));
                 asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -349,7 +405,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
             if (__syncthreads_or(!ok)) {
                 // the copies never landed: record it, let them finish (bounded), leave
                 if (threadIdx.x == 0) {
-                    atomicOr(tp.err, 1u);
+                    atomicOr(p.err, 1u);
                     mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
                 }
                 __syncthreads();
@@ -473,6 +529,34 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
         const int ne = bytes / esz;
 
         if (bytes > 0) {
+            if constexpr (kChecked) {
+                // every widened copy inside the tile's segment of its row (or of w),
+                // the stores inside the segment, the reduce-scatter's inside chunk c
+                if (threadIdx.x == 0) {
+                    bool ok = sg.begin >= 0 && sg.end <= p.p && first >= sg.begin && first + ne <= sg.end;
+                    for (int k = 0; k < n; ++k) {
+                        const char *a = reinterpret_cast<const char *>(p.rows[k]) + first * esz;
+                        const int d = (int)(reinterpret_cast<uintptr_t>(a) & 15);
+                        ok = ok && span_in(a - d, (d + bytes + 15) & ~15,
+                                           reinterpret_cast<const char *>(p.rows[k]) + sg.begin * esz,
+                                           (sg.end - sg.begin) * esz);
+                    }
+                    if constexpr (OUT == kOutAllSgd) {
+                        const char *a = reinterpret_cast<const char *>(p.w + first);
+                        const int d = (int)(reinterpret_cast<uintptr_t>(a) & 15);
+                        ok = ok && span_in(a - d, (d + ne * 4 + 15) & ~15, p.w + sg.begin, (sg.end - sg.begin) * 4);
+                    }
+                    if constexpr (OUT == kOutOne) {
+                        int64_t b, e;
+                        chunk_span(p.p, p.n, c, &b, &e);
+                        ok = ok && first >= b && first + ne <= e;
+                    }
+                    if (!ok) atomicOr(p.err, kErrBounds);
+                    reinterpret_cast<int *>(bar + 1)[0] = ok ? 0 : 1;  // the spare half of the barrier's slot
+                }
+                __syncthreads();
+                if (reinterpret_cast<volatile int *>(bar + 1)[0]) return;
+            }
             if (threadIdx.x == 0) {
                 uint32_t total = 0;
                 for (int k = 0; k < n; ++k) {
@@ -508,7 +592,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
             if (__syncthreads_or(!ok)) {
                 // the copies never landed: record it, let them finish (bounded), leave
                 if (threadIdx.x == 0) {
-                    atomicOr(tp.err, 1u);
+                    atomicOr(p.err, 1u);
                     mbar_wait_bounded(smem_addr(bar), 0, kWaitLimitNs);
                 }
                 __syncthreads();
@@ -615,6 +699,9 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
 struct StagedParams {
     void *rows[RA_MAX_N];
     float *msg;  // binary32 partial sums (bf16 only), element i at msg[i]
+    const char *msg_lo, *msg_hi;  // the workspace holding them (checked build)
+    unsigned int *err;            // the device's error word (checked build)
+    int64_t p;                    // elements per row (checked build)
     int n;
     int t;       // iteration
     int op;      // StagedOp
@@ -628,8 +715,18 @@ struct StagedParams {
 // (c + t) mod n in scatter-reduce iteration t and moves to (c + t + 1) mod n;
 // the complete chunk sits at worker (c - 1) mod n; in all-gather iteration t
 // worker (c + t - 1) mod n sends it to worker (c + t) mod n.
+__device__ __forceinline__ bool staged_in_bounds(const StagedParams &p, int64_t i, int count) {
+    // elements [i, i + count) of the rows, and of the workspace when in use
+    bool ok = i >= 0 && i + count <= p.p;
+    if (p.msg) ok = ok && span_in(p.msg + i, (int64_t)count * 4, p.msg_lo, p.msg_hi - p.msg_lo);
+    if (!ok) atomicOr(p.err, kErrBounds);
+    return ok;
+}
+
 template <class E>
 __device__ __forceinline__ void staged_scalar(const StagedParams &p, int c, int64_t i) {
+    if constexpr (kChecked)
+        if (!staged_in_bounds(p, i, 1)) return;
     const int n = p.n;
     switch (p.op) {
         case kOpScatter: {  // receiver's own value + received partial
@@ -670,6 +767,8 @@ template <class E>
 __device__ __forceinline__ void staged_vector(const StagedParams &p, int c, int64_t i) {
     const int n = p.n;
     constexpr int V = E::kVec;
+    if constexpr (kChecked)
+        if (!staged_in_bounds(p, i, V)) return;
     constexpr int esz = (int)sizeof(typename E::T);
     switch (p.op) {
         case kOpScatter: {
@@ -771,6 +870,7 @@ struct GatherParams {
     int mis;
     int skip_owner;       // 1: the source is the owner's own array, which is not rewritten
     unsigned int *err;    // the device's error word: bit 0 = a bounded wait gave up
+    int64_t p;            // elements per row (checked build)
     int64_t ntiles;
     Seg seg[RA_MAX_N];
 };
@@ -778,6 +878,14 @@ struct GatherParams {
 template <class E>
 __device__ __forceinline__ void gather_scalar(const GatherParams &p, int c, int64_t i) {
     using T = typename E::T;
+    if constexpr (kChecked) {
+        int64_t b, e;
+        chunk_span(p.p, p.n, c, &b, &e);
+        if (!(i >= b && i < e && i < p.p)) {
+            atomicOr(p.err, kErrBounds);
+            return;
+        }
+    }
     const T v = reinterpret_cast<const T *>(p.src[c])[i];
     const int owner = c == 0 ? p.n - 1 : c - 1;
     for (int k = 0; k < p.n; ++k)
@@ -823,6 +931,23 @@ __global__ void __launch_bounds__(32) all_gather_tma_kernel(const __grid_constan
         const int64_t left = (ae - first) * esz;
         const int bytes = left <= 0 ? 0 : (int)(left < B ? left : B);
         int fail = 0;
+        if constexpr (kChecked) {
+            // the owner's chunk c in the source, every destination row
+            if (bytes > 0 && threadIdx.x == 0) {
+                int64_t b, e;
+                chunk_span(p.p, p.n, c, &b, &e);
+                bool ok = span_in(reinterpret_cast<const char *>(p.src[c]) + first * esz, bytes,
+                                  reinterpret_cast<const char *>(p.src[c]) + b * esz, (e - b) * esz);
+                for (int k = 0; k < p.n; ++k)
+                    ok = ok && span_in(reinterpret_cast<const char *>(p.rows[k]) + first * esz, bytes, p.rows[k],
+                                       p.p * esz);
+                if (!ok) {
+                    atomicOr(p.err, kErrBounds);
+                    fail = 2;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, fail, 0)) return;
+        }
         if (bytes > 0 && threadIdx.x == 0) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(smem_addr(bar)));
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

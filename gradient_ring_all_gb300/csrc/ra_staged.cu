@@ -11,6 +11,10 @@ static cudaError_t staged_launch_one(const StagedLaunch &L, int op, int t, cudaS
     memset(&p, 0, sizeof(p));
     for (int k = 0; k < L.n; ++k) p.rows[k] = L.rows[k];
     p.msg = L.msg;
+    p.msg_lo = L.msg_lo;
+    p.msg_hi = L.msg_hi;
+    p.err = L.err;
+    p.p = L.p;
     p.n = L.n;
     p.t = t;
     p.op = op;
@@ -43,6 +47,7 @@ static cudaError_t gather_scalar_launch(const GatherLaunch &L, cudaStream_t s) {
     p.mis = L.mis;
     p.skip_owner = L.skip_owner ? 1 : 0;
     p.err = L.err;
+    p.p = L.p;
     p.ntiles = L.ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
     const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
@@ -62,6 +67,7 @@ static cudaError_t gather_tma_launch(const GatherLaunch &L, cudaStream_t s) {
     p.mis = L.mis;
     p.skip_owner = L.skip_owner ? 1 : 0;
     p.err = L.err;
+    p.p = L.p;
     p.ntiles = L.ntiles;
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
     const size_t smem = (size_t)kGatherTileBytes + 16;

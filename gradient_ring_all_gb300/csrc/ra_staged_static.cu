@@ -138,6 +138,14 @@ extern "C" ra_status ra_allreduce_avg_staged_static(void *const *bufs, int n, in
     // partial sums at scratch + shift, so that msg + i is 16-byte aligned
     // exactly when the rows' element i starts a vector
     prm.msg = dtype == RA_BF16 ? d.scratch + (vec ? mis % 4 : 0) : nullptr;
+    prm.msg_lo = reinterpret_cast<const char *>(d.scratch);
+    prm.msg_hi = reinterpret_cast<const char *>(d.scratch + RA_STAGED_STATIC_MAX_P + 4);
+    prm.p = p;
+    e = device_error_word(&prm.err);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return RA_ERR_CUDA;
+    }
     int nseg = 0;
     for (int c = 0; c < n; ++c) {
         const int64_t b = (int64_t)c * q + (c < r ? c : r), len = q + (c < r ? 1 : 0);

@@ -74,7 +74,8 @@ typedef enum {
     RA_ERR_UNSUPPORTED = 2, /* a valid request outside what the called function handles (see its notes) */
     RA_ERR_OVERLAP = 3,     /* two buffers (or w and a buffer) share bytes */
     RA_ERR_CUDA = 4,        /* a CUDA call failed; see ra_last_cuda_error() */
-    RA_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait gave up */
+    RA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
+    RA_ERR_BOUNDS = 6       /* bounds-checked build only: a kernel found a range outside the caller's buffers */
 } ra_status;
 
 /* A contiguous element range [offset, offset + count) of every worker's array. */
@@ -330,12 +331,28 @@ ra_status ra_reducer_destroy(ra_reducer *r);
  * copies (global -> shared memory) on an mbarrier; each wait is limited to
  * 2 s (the copies of one tile take microseconds), after which the kernel
  * records the failure in the device's error word, skips its stores and
- * returns, so the context stays usable.  Returns RA_ERR_TIMEOUT if such a record exists (the
- * results of the calls in flight at the time are then invalid), RA_OK
- * otherwise, and clears the record.  Reads device memory synchronously:
- * call it after the streams in question have finished.
+ * returns, so the context stays usable.  Returns RA_ERR_TIMEOUT if such a
+ * record exists (the results of the calls in flight at the time are then
+ * invalid), RA_ERR_BOUNDS if the bounds-checked build recorded an access
+ * outside the caller's buffers (see ra_selftest_bounds_check; it takes
+ * precedence), RA_OK otherwise, and clears the record.  Reads device memory
+ * synchronously: call it after the streams in question have finished.
  */
 ra_status ra_check_device_errors(void);
+
+/*
+ * ra_selftest_bounds_check -- the bounds-checked build (libgradient_ring_all_
+ * checked.so, built for the tests) verifies inside every kernel that each
+ * global range it reads or writes lies in the caller's buffers, skips the
+ * access otherwise, and records RA_ERR_BOUNDS for ra_check_device_errors().
+ * This call exercises that check: it runs the fused all-reduce over the p
+ * elements of `bufs` (arguments as ra_allreduce_avg) while telling the
+ * kernel that the rows hold only p - 1 elements, so the tile holding the
+ * last element must be reported and skipped.  No memory outside the rows
+ * is touched; the rows' contents afterwards are unspecified.  Needs p >= 2
+ * and n >= 2.  The product build returns RA_ERR_UNSUPPORTED.
+ */
+ra_status ra_selftest_bounds_check(void *const *bufs, int n, int64_t p, int dtype, void *stream);
 
 /*
  * ra_selftest_wait_timeout -- exercises that timeout path on purpose: queues

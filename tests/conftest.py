@@ -19,3 +19,17 @@ def _build_host_libs():
     import synth
     oracle.build()
     synth.build()
+
+
+@pytest.fixture(autouse=True)
+def _no_out_of_bounds_access(request):
+    # Under the bounds-checked build (GRADIENT_RING_ALL_CHECKED=1) every GPU
+    # test must leave no record of a kernel touching memory outside the
+    # caller's buffers.
+    yield
+    if os.environ.get("GRADIENT_RING_ALL_CHECKED") != "1" or request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    import gradient_ring_all_gb300 as ra
+    torch.cuda.synchronize()
+    assert ra.ra_check_device_errors() != ra.RA_ERR_BOUNDS, "a kernel accessed memory outside the caller's buffers"
