@@ -126,11 +126,12 @@ __host__ __device__ inline void unaligned_interior(int64_t b, int64_t e, int V, 
     if (*ae < *ab) *ab = *ae = b;
 }
 // shared memory of the unaligned kernel: a slot of B + 16 bytes per row
-// (room for the widening), a weight slot for SGD, the mbarrier, and the
-// per-row byte offsets
+// (room for the widening), a weight slot for SGD, the mbarrier, the per-row
+// byte offsets and staging offsets, and (8-byte aligned) the rows' tile
+// pointers
 inline size_t unaligned_smem_bytes(int n, int tile_bytes, int out, int esz) {
     return (size_t)n * ((size_t)tile_bytes + 16) + (out == kOutAllSgd ? (size_t)(tile_bytes / esz) * 4 + 16 : 0) + 16 +
-           (size_t)(n + 1) * sizeof(int);
+           (size_t)(2 * n + 1) * sizeof(int) + 8 + (size_t)n * sizeof(char *);
 }
 int64_t fused_unaligned_assign_tiles(Seg *seg, int nseg, int dtype, int tile_bytes);
 

@@ -514,6 +514,13 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
     const int wslot_bytes = OUT == kOutAllSgd ? (B / esz) * 4 + 16 : 0;
     uint64_t *bar = reinterpret_cast<uint64_t *>(wslot + wslot_bytes);
     int *shift = reinterpret_cast<int *>(wslot + wslot_bytes + 16);  // d_k of row k; shift[n]: the weights'
+    // per tile: where row k's elements start in shared memory, and row k's
+    // first element of the tile in global memory (set by thread 0, so that
+    // the fold and the stores do no per-row address arithmetic: measured
+    // +2.5 % for bf16 at n=16, +0.2-0.3 % in binary32)
+    int *rowoff = shift + n + 1;
+    char **rowptr = reinterpret_cast<char **>(
+        (reinterpret_cast<uintptr_t>(rowoff + n) + 7) & ~static_cast<uintptr_t>(7));
     pdl_enter();
 
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
@@ -562,6 +569,8 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
                 for (int k = 0; k < n; ++k) {
                     const int d = (int)((reinterpret_cast<uintptr_t>(p.rows[k]) + (uintptr_t)first * esz) & 15);
                     shift[k] = d;
+                    rowoff[k] = k * slot + d;
+                    rowptr[k] = reinterpret_cast<char *>(p.rows[k]) + first * esz;
                     total += (uint32_t)((d + bytes + 15) & ~15);
                 }
                 if constexpr (OUT == kOutAllSgd) {
@@ -600,18 +609,8 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
             }
             for (int j0 = threadIdx.x; j0 < ne; j0 += J * kThreads) {
                 float acc[J];
-                {
-                    const unsigned char *b = smem + (size_t)c * slot + shift[c];
-#pragma unroll
-                    for (int u = 0; u < J; ++u) {
-                        const int j = j0 + u * kThreads;
-                        acc[u] = j < ne ? ld_staged<T>(b + j * esz) : 0.f;
-                    }
-                }
-                int r = c;
-                for (int k = 1; k < n; ++k) {
-                    r = r + 1 == n ? 0 : r + 1;
-                    const unsigned char *b = smem + (size_t)r * slot + shift[r];
+                auto add_row = [&](int r) {
+                    const unsigned char *b = smem + rowoff[r];
 #pragma unroll
                     for (int u = 0; u < J; ++u) {
                         const int j = j0 + u * kThreads;
@@ -620,7 +619,18 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
                             if constexpr (OUT == kOutAllWire) acc[u] = round_bf16(acc[u]);
                         }
                     }
+                };
+                {
+                    const unsigned char *b = smem + rowoff[c];
+#pragma unroll
+                    for (int u = 0; u < J; ++u) {
+                        const int j = j0 + u * kThreads;
+                        acc[u] = j < ne ? ld_staged<T>(b + j * esz) : 0.f;
+                    }
                 }
+                // ring order from row c: c + 1 .. n - 1, then 0 .. c - 1
+                for (int r = c + 1; r < n; ++r) add_row(r);
+                for (int r = 0; r < c; ++r) add_row(r);
                 T v[J];
                 float held[J];
 #pragma unroll
@@ -641,7 +651,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
                         if (j0 + u * kThreads < ne) put_elem<T>(base + (j0 + u * kThreads) * esz, v[u]);
                 } else {
                     for (int k = 0; k < n; ++k) {
-                        char *base = reinterpret_cast<char *>(p.rows[k]) + first * esz;
+                        char *base = rowptr[k];
 #pragma unroll
                         for (int u = 0; u < J; ++u)
                             if (j0 + u * kThreads < ne) put_elem<T>(base + (j0 + u * kThreads) * esz, v[u]);

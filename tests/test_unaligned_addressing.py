@@ -60,7 +60,7 @@ def walk(n, esz, rows, out, segs, w, aux, budget, margin=True):
     B = tile_bytes(n, out == "one", budget)
     slot = B + 16
     wslot = (B // esz) * 4 + 16 if out == "sgd" else 0
-    assert n * slot + wslot + 16 + 4 * (n + 1) <= 227 * 1024
+    assert n * slot + wslot + 16 + 4 * (2 * n + 1) + 8 + 8 * n <= 227 * 1024
     written = {}
 
     def wr(dest, lo, hi):
