@@ -29,7 +29,16 @@ static_assert(sizeof(Seg) == 32, "Seg layout");
 constexpr int kThreadsPerBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;  // largest gridDim.x
 constexpr int kScalarPerThread = 4;  // elements per thread per tile, scalar staged and gather paths
-constexpr int kStagedTileVec = 512;  // 16-byte vectors per tile, staged kernel
+// 16-byte vectors per tile of the staged kernel, 4 per thread.  Measured on
+// GB300 (staged ring, GB/s over its schedule's bytes): 512 / 1024 / 2048 /
+// 4096 gave 6921 / 7019 / 6984 / 6901 at n=8 binary32, 6947 / 7001 / 6949 /
+// 6879 at n=16 bf16 and 6720 / 6876 / 6294 / 5592 at n=32.  Loading all of a
+// thread's vectors before any store (the rows may alias, so the compiler
+// keeps them in order) was slower: 6520 at n=8, 5576 at n=16 bf16.
+#ifndef RA_STAGED_TILE_VEC
+#define RA_STAGED_TILE_VEC 1024
+#endif
+constexpr int kStagedTileVec = RA_STAGED_TILE_VEC;
 
 // The 16-byte-vector interior [ab, ae) of the element range [b, e) when the
 // rows' addresses are `mis` elements past a 16-byte boundary (V elements per
