@@ -199,7 +199,7 @@ int64_t fused_tma_assign_tiles(Seg *seg, int nseg, int dtype, int mis, int tile_
     return t;
 }
 
-int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis) {
+int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis, int tile_vec) {
     const int V = vec_elems(dtype);
     const int64_t ts = (int64_t)kThreadsPerBlock * kScalarPerThread;
     int64_t t = 0;
@@ -209,7 +209,7 @@ int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis)
         if (vector) {
             int64_t ab, ae;
             vector_interior(seg[k].begin, seg[k].end, mis, V, &ab, &ae);
-            tiles = std::max<int64_t>(1, ((ae - ab) / V + kStagedTileVec - 1) / kStagedTileVec);
+            tiles = std::max<int64_t>(1, ((ae - ab) / V + tile_vec - 1) / tile_vec);
         } else {
             tiles = std::max<int64_t>(1, (seg[k].end - seg[k].begin + ts - 1) / ts);
         }
@@ -323,7 +323,8 @@ ra_status ra_allreduce_avg_staged(void *const *bufs, int n, int64_t p, int dtype
     }
     std::vector<Seg> segs;
     ring_segments(0, p, n, &segs);
-    L.ntiles = staged_assign_tiles(segs.data(), (int)segs.size(), dtype, L.vector, mis);
+    L.tile_vec = staged_tile_vec(p / vec_elems(dtype));
+    L.ntiles = staged_assign_tiles(segs.data(), (int)segs.size(), dtype, L.vector, mis, L.tile_vec);
     L.seg = segs.data();
     L.nseg = (int)segs.size();
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -485,7 +486,7 @@ ra_status ra_all_gather(void *const *bufs, int n, int64_t p, int dtype, void *co
     std::vector<Seg> segs;
     ring_segments(0, p, n, &segs);
     L.ntiles = L.vector ? fused_tma_assign_tiles(segs.data(), (int)segs.size(), dtype, mis, kGatherTileBytes)
-                        : staged_assign_tiles(segs.data(), (int)segs.size(), dtype, false, mis);
+                        : staged_assign_tiles(segs.data(), (int)segs.size(), dtype, false, mis, 0);
     L.seg = segs.data();
     L.nseg = (int)segs.size();
     cudaError_t e = device_error_word(&L.err);

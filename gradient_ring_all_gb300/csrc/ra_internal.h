@@ -29,16 +29,21 @@ static_assert(sizeof(Seg) == 32, "Seg layout");
 constexpr int kThreadsPerBlock = 256;
 constexpr int64_t kMaxGrid = 0x7fffffff;  // largest gridDim.x
 constexpr int kScalarPerThread = 4;  // elements per thread per tile, scalar staged and gather paths
-// 16-byte vectors per tile of the staged kernel, 4 per thread.  Measured on
+// 16-byte vectors per tile of the staged kernel: 1024 (4 per thread) when a
+// launch still fills a wave of blocks with them, else 512.  Measured on
 // GB300 (staged ring, GB/s over its schedule's bytes): 512 / 1024 / 2048 /
 // 4096 gave 6921 / 7019 / 6984 / 6901 at n=8 binary32, 6947 / 7001 / 6949 /
-// 6879 at n=16 bf16 and 6720 / 6876 / 6294 / 5592 at n=32.  Loading all of a
+// 6879 at n=16 bf16 and 6720 / 6876 / 6294 / 5592 at n=32; but the 1M-element
+// ring (256 blocks of 1024) slowed to 38 us, against 28 with 512 and 29 with
+// 256 vectors per tile.  The tile size is a template parameter: with a
+// runtime loop bound the large cases lost 2-3 %.  Loading all of a
 // thread's vectors before any store (the rows may alias, so the compiler
 // keeps them in order) was slower: 6520 at n=8, 5576 at n=16 bf16.
-#ifndef RA_STAGED_TILE_VEC
-#define RA_STAGED_TILE_VEC 1024
-#endif
-constexpr int kStagedTileVec = RA_STAGED_TILE_VEC;
+constexpr int kStagedTileVecLarge = 1024, kStagedTileVecSmall = 512;
+constexpr int64_t kStagedWaveBlocks = 152 * 8;  // SMs x resident blocks of 256 threads
+inline int staged_tile_vec(int64_t vectors) {
+    return vectors / kStagedTileVecLarge >= kStagedWaveBlocks ? kStagedTileVecLarge : kStagedTileVecSmall;
+}
 
 // The 16-byte-vector interior [ab, ae) of the element range [b, e) when the
 // rows' addresses are `mis` elements past a 16-byte boundary (V elements per
@@ -153,7 +158,7 @@ cudaError_t device_error_word(unsigned int **out);
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, unsigned int *err, cudaStream_t s);
 
 // fill seg[].tile0 and return the tile count of the staged kernel
-int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis);
+int64_t staged_assign_tiles(Seg *seg, int nseg, int dtype, bool vector, int mis, int tile_vec);
 
 cudaError_t launch_fused_f32(const FusedLaunch &L, int64_t ntiles, cudaStream_t s);
 cudaError_t launch_fused_bf16(const FusedLaunch &L, int64_t ntiles, cudaStream_t s);
@@ -172,6 +177,7 @@ struct StagedLaunch {
     const Seg *seg;
     int nseg;
     int64_t ntiles;
+    int tile_vec;  // vector mode: 16-byte vectors per tile (staged_tile_vec)
 };
 cudaError_t launch_staged_step(const StagedLaunch &L, int op, int t, cudaStream_t s);
 

@@ -837,7 +837,7 @@ __device__ __forceinline__ void staged_vector(const StagedParams &p, int c, int6
     }
 }
 
-template <class E, bool VECTOR>
+template <class E, bool VECTOR, int TV>
 __global__ void __launch_bounds__(kThreads) staged_step_kernel(const __grid_constant__ StagedParams p) {
     constexpr int V = E::kVec;
     pdl_enter();
@@ -848,9 +848,9 @@ __global__ void __launch_bounds__(kThreads) staged_step_kernel(const __grid_cons
         if constexpr (VECTOR) {
             int64_t ab, ae;
             vector_interior(sg.begin, sg.end, p.mis, V, &ab, &ae);
-            const int64_t i0 = ab + (t_in_seg * kStagedTileVec + threadIdx.x) * V;
+            const int64_t i0 = ab + (t_in_seg * TV + threadIdx.x) * V;
 #pragma unroll
-            for (int j = 0; j < kStagedTileVec / kThreads; ++j) {
+            for (int j = 0; j < TV / kThreads; ++j) {
                 const int64_t i = i0 + (int64_t)j * kThreads * V;
                 if (i < ae) staged_vector<E>(p, sg.c, i);
             }

@@ -24,7 +24,9 @@ static cudaError_t staged_launch_one(const StagedLaunch &L, int op, int t, cudaS
     for (int k = 0; k < L.nseg; ++k) p.seg[k] = L.seg[k];
     // one tile per block, as for the fused kernel
     const int64_t grid = L.ntiles < kMaxGrid ? L.ntiles : kMaxGrid;
-    return launch_pdl(staged_step_kernel<E, VEC>, grid, kThreadsPerBlock, 0, s, p);
+    if (VEC && L.tile_vec == kStagedTileVecLarge)
+        return launch_pdl(staged_step_kernel<E, VEC, kStagedTileVecLarge>, grid, kThreadsPerBlock, 0, s, p);
+    return launch_pdl(staged_step_kernel<E, VEC, kStagedTileVecSmall>, grid, kThreadsPerBlock, 0, s, p);
 }
 
 cudaError_t launch_staged_step(const StagedLaunch &L, int op, int t, cudaStream_t s) {

@@ -57,14 +57,16 @@ cudaError_t setup_device(int dev, DeviceSetup *out) {
 
 // one tile per block, as for the other staged launches
 template <class E, bool VEC>
-cudaError_t launch_step(const StagedParams &p, cudaStream_t s) {
+cudaError_t launch_step(const StagedParams &p, int tile_vec, cudaStream_t s) {
     const int64_t grid = p.ntiles < kMaxGrid ? p.ntiles : kMaxGrid;
-    return launch_pdl(staged_step_kernel<E, VEC>, grid, kThreadsPerBlock, 0, s, p);
+    if (VEC && tile_vec == kStagedTileVecLarge)
+        return launch_pdl(staged_step_kernel<E, VEC, kStagedTileVecLarge>, grid, kThreadsPerBlock, 0, s, p);
+    return launch_pdl(staged_step_kernel<E, VEC, kStagedTileVecSmall>, grid, kThreadsPerBlock, 0, s, p);
 }
 
-cudaError_t launch_step_any(const StagedParams &p, int dtype, bool vec, cudaStream_t s) {
-    if (dtype == RA_F32) return vec ? launch_step<F32, true>(p, s) : launch_step<F32, false>(p, s);
-    return vec ? launch_step<BF16, true>(p, s) : launch_step<BF16, false>(p, s);
+cudaError_t launch_step_any(const StagedParams &p, int dtype, bool vec, int tile_vec, cudaStream_t s) {
+    if (dtype == RA_F32) return vec ? launch_step<F32, true>(p, tile_vec, s) : launch_step<F32, false>(p, tile_vec, s);
+    return vec ? launch_step<BF16, true>(p, tile_vec, s) : launch_step<BF16, false>(p, tile_vec, s);
 }
 
 }  // namespace
@@ -152,23 +154,24 @@ extern "C" ra_status ra_allreduce_avg_staged_static(void *const *bufs, int n, in
         if (len > 0) prm.seg[nseg++] = Seg{b, b + len, 0, c, 0};
     }
     prm.nseg = nseg;
-    prm.ntiles = staged_assign_tiles(prm.seg, nseg, dtype, vec, prm.mis);
+    const int tile_vec = staged_tile_vec(p / V);
+    prm.ntiles = staged_assign_tiles(prm.seg, nseg, dtype, vec, prm.mis, tile_vec);
 
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int t = 0; t < n - 1 && e == cudaSuccess; ++t) {
         prm.op = kOpScatter;
         prm.t = t;
-        e = launch_step_any(prm, dtype, vec, s);
+        e = launch_step_any(prm, dtype, vec, tile_vec, s);
     }
     if (e == cudaSuccess) {
         prm.op = kOpDivide;
         prm.t = 0;
-        e = launch_step_any(prm, dtype, vec, s);
+        e = launch_step_any(prm, dtype, vec, tile_vec, s);
     }
     for (int t = 0; t < n - 1 && e == cudaSuccess; ++t) {
         prm.op = kOpGather;
         prm.t = t;
-        e = launch_step_any(prm, dtype, vec, s);
+        e = launch_step_any(prm, dtype, vec, tile_vec, s);
     }
     if (e != cudaSuccess) {
         record_cuda_error(e);
