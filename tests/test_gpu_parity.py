@@ -197,6 +197,25 @@ def test_staged_matches_oracle_and_counts_traffic(n, p, dtype, layout):
     assert [t[1] for t in traffic] == recv.tolist()
 
 
+@pytest.mark.parametrize("n,p,dtype,layout", [(8, 6_000_017, "f32", "separate"), (4, 10_500_013, "bf16", "offset"),
+                                              (4, 10_500_013, "f32", "offset")])
+def test_staged_large_tiles_match_oracle(n, p, dtype, layout):
+    # large enough that each launch fills a wave with 1024-vector tiles (the
+    # staged kernel's larger tile instance); also the workspace-free variant
+    host = _host_rows(n, p, dtype, seed=190 + n)
+    rows_o = [r.copy() for r in host]
+    (oracle.ring_allreduce_avg_f32 if dtype == "f32" else oracle.ring_allreduce_avg_bf16)(rows_o)
+    rows = to_device_rows(host, layout=layout, pad=3)
+    ra.ra_allreduce_avg_staged(rows)
+    torch.cuda.synchronize()
+    _assert_rows_equal_oracle(rows, rows_o[0])
+    if dtype == "f32":  # binary32 needs no scratch, so any length works without a workspace
+        rows = to_device_rows(host, layout=layout, pad=3)
+        ra.ra_allreduce_avg_staged_static(rows)
+        torch.cuda.synchronize()
+        _assert_rows_equal_oracle(rows, rows_o[0])
+
+
 def test_staged_equals_fused():
     wl = synth.WORKLOADS["ring4_uneven_1m_f32"]
     host = [wl.row(k) for k in range(wl.n)]
