@@ -148,3 +148,20 @@ def test_every_call_rejects_bad_arguments_on_the_host(lib):
     assert lib.ra_bucket_plan(three, 3, 4, 400, out, 1, ctypes.byref(nb)) == INVALID              # max_out too small
     lib.ra_selftest_wait_timeout.argtypes = [ctypes.c_int, vp]
     assert lib.ra_selftest_wait_timeout(0, None) == INVALID
+
+
+def test_bounds_selftest_on_the_host(lib):
+    # the product library checks the arguments, then answers the bounds
+    # self-test with RA_ERR_UNSUPPORTED (only the checked build runs it);
+    # none of these reaches CUDA
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.ra_selftest_bounds_check.argtypes = [ctypes.POINTER(vp), ctypes.c_int, i64, ctypes.c_int, vp]
+    INVALID, UNSUPPORTED, OVERLAP = 1, 2, 3
+    rows = (vp * 2)(0x100000, 0x200000)
+    assert lib.ra_selftest_bounds_check(None, 2, 1000, 0, None) == INVALID
+    assert lib.ra_selftest_bounds_check(rows, 1, 1000, 0, None) == INVALID      # n < 2
+    assert lib.ra_selftest_bounds_check(rows, 2, 1, 0, None) == INVALID         # p < 2
+    assert lib.ra_selftest_bounds_check(rows, 2, 300000, 0, None) == OVERLAP    # 1.2 MB rows 1 MiB apart
+    assert lib.ra_selftest_bounds_check(rows, 2, 1000, 0, None) == UNSUPPORTED
+    lib.ra_status_str.restype = ctypes.c_char_p
+    assert lib.ra_status_str(6) == b"RA_ERR_BOUNDS"
