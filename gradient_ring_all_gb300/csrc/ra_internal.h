@@ -92,7 +92,8 @@ struct FusedLaunch {
 
 // Tile size of the fused kernels: bytes of each row one block stages in
 // shared memory.  The n staged rows take about a budget per block --
-// RA_TMA_STAGE_BYTES for the vector path, more for the unaligned kernel,
+// RA_TMA_STAGE_BYTES for the vector path (RA_TMA_STAGE_BYTES_NPOT when n is
+// not a power of two), more for the unaligned kernel,
 // which holds its tile longer, and 64 KB for the reduce-scatter, which writes
 // one row per tile instead of n -- with the tile a multiple of 16 bytes
 // between 2 KB and 16 KB, and at most RA_TMA_MAX_STAGE_BYTES staged per
@@ -108,6 +109,12 @@ struct FusedLaunch {
 #ifndef RA_TMA_STAGE_BYTES
 #define RA_TMA_STAGE_BYTES 16384
 #endif
+// worker counts that are not powers of two stage more per block: n=3/5/7
+// binary32 7.12/7.14/7.12 TB/s at 24 KB against 6.90/7.01/6.91 at 16 KB,
+// while n=8 lost 0.2 % at 24 KB (from n=12 on the 2 KB minimum decides)
+#ifndef RA_TMA_STAGE_BYTES_NPOT
+#define RA_TMA_STAGE_BYTES_NPOT 24576
+#endif
 constexpr int64_t kTmaStageBytesOneOut = 65536;
 #ifndef RA_UNALIGNED_STAGE_BYTES
 #define RA_UNALIGNED_STAGE_BYTES 32768
@@ -119,7 +126,11 @@ constexpr int64_t kTmaStageBytesOneOut = 65536;
 #define RA_TMA_MAX_STAGE_BYTES 65536
 #endif
 inline int fused_tile_bytes(int n, bool one_destination, bool vector) {
-    const int64_t budget = one_destination ? kTmaStageBytesOneOut : vector ? RA_TMA_STAGE_BYTES : RA_UNALIGNED_STAGE_BYTES;
+    const bool pow2 = (n & (n - 1)) == 0;
+    const int64_t budget = one_destination ? kTmaStageBytesOneOut
+                           : !vector       ? RA_UNALIGNED_STAGE_BYTES
+                           : pow2          ? RA_TMA_STAGE_BYTES
+                                           : RA_TMA_STAGE_BYTES_NPOT;
     int64_t b = (budget / n) & ~(int64_t)15;
     if (b < RA_TMA_MIN_TILE_BYTES) b = RA_TMA_MIN_TILE_BYTES;
     if (b > 16384) b = 16384;
