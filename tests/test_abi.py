@@ -165,3 +165,54 @@ def test_bounds_selftest_on_the_host(lib):
     assert lib.ra_selftest_bounds_check(rows, 2, 1000, 0, None) == UNSUPPORTED
     lib.ra_status_str.restype = ctypes.c_char_p
     assert lib.ra_status_str(6) == b"RA_ERR_BOUNDS"
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "ring_allreduce.h"
+
+int main(void) {
+    int64_t b, e;
+    ra_bucket plan[8];
+    int nb = 0, k;
+    int64_t numel[5] = {100, 200, 300, 50, 7};
+    void *bufs[2];
+    ra_chunk_range(1048579, 4, 3, &b, &e);
+    printf("chunk %lld %lld\n", (long long)b, (long long)e);
+    if (ra_bucket_plan(numel, 5, 4, 1000, plan, 8, &nb) != RA_OK) return 2;
+    printf("buckets %d", nb);
+    for (k = 0; k < nb; ++k) printf(" %lld:%lld", (long long)plan[k].offset, (long long)plan[k].count);
+    printf("\n");
+    bufs[0] = (void *)0x100000;
+    bufs[1] = (void *)0x100020;  /* 40-byte rows 32 bytes apart */
+    printf("overlap %d\n", (int)ra_allreduce_avg(bufs, 2, 10, RA_F32, NULL));
+    printf("%s\n", ra_status_str(RA_ERR_BOUNDS));
+    return 0;
+}
+"""
+
+
+def test_the_header_is_c_and_links(lib):
+    # a C99 program against the header and the library, host-only calls
+    import subprocess
+    import oracle
+    d = os.path.join(ROOT, "tests", ".scratch", "c_abi")
+    os.makedirs(d, exist_ok=True)
+    src, exe = os.path.join(d, "abi.c"), os.path.join(d, "abi")
+    with open(src, "w") as f:
+        f.write(C_PROGRAM)
+    libdir = os.path.join(ROOT, "gradient_ring_all_gb300", "lib")
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                        os.path.join(ROOT, "include"), src, "-o", exe, "-L", libdir, "-lgradient_ring_all",
+                        "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    lines = out.stdout.split("\n")
+    assert lines[0] == "chunk 786435 1048579"
+    want = oracle.bucket_plan([100, 200, 300, 50, 7], 4, 1000)
+    assert lines[1] == "buckets %d" % len(want) + "".join(" %d:%d" % (o, c) for o, c in want)
+    assert lines[2] == "overlap 3"
+    assert lines[3] == "RA_ERR_BOUNDS"
+    import shutil
+    shutil.rmtree(d, ignore_errors=True)
