@@ -1,0 +1,54 @@
+"""Host-side helpers of bench.py (no GPU): the source hash that keys the
+committed ncu traffic figures follows the code, not its comments (the bench
+reports the traffic only while the hash matches); the two arms print the
+same config object; call_bytes follows each call's design."""
+from __future__ import annotations
+
+import os
+import shutil
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import synth  # noqa: E402
+
+
+def _copy_csrc(tag):
+    d = os.path.join(ROOT, "tests", ".scratch", "csrc_" + tag)
+    shutil.rmtree(d, ignore_errors=True)
+    shutil.copytree(os.path.join(ROOT, "gradient_ring_all_gb300", "csrc"), d)
+    return d
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    base = bench._source_hash()
+    d = _copy_csrc("comments")
+    try:
+        assert bench._source_hash(d) == base
+        f = os.path.join(d, "ra_kernels.cuh")
+        src = open(f).read()
+        open(f, "w").write("// a new comment\n/* and a block\n comment */\n" + src.replace("\n", "\n  ", 3))
+        assert bench._source_hash(d) == base  # comments and indentation only
+        open(f, "w").write(src.replace("kWaitLimitNs = 2000000000ull", "kWaitLimitNs = 1000000000ull"))
+        assert bench._source_hash(d) != base  # a code change
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+
+
+def test_both_arms_print_one_config():
+    wl = synth.WORKLOADS["speech300m_n8_f32"]
+    c = bench._config(wl, wl.n, wl.p, 1)
+    assert c["workload"] == "speech300m_n8_f32" and c["workers"] == 8 and c["elements_per_worker"] == 300_000_000
+    assert c["bytes_per_step"] == 19_200_000_000 and c["parallelism"] == "single GPU"
+    assert bench._config(wl, wl.n, wl.p, 4)["parallelism"] == "replicas"
+
+
+def test_call_bytes():
+    n, p = 8, 300_000_000
+    assert bench.call_bytes("allreduce", n, p, 4) == 2 * n * p * 4
+    assert bench.call_bytes("sgd", n, p, 4) == 2 * n * p * 4 + 2 * p * 4
+    assert bench.call_bytes("reduce_scatter", n, p, 4) == (n + 1) * p * 4
+    assert bench.call_bytes("all_gather", n, p, 4) == n * p * 4
+    assert bench.call_bytes("staged", n, p, 4) == 44_400_000_000  # (5(N-1)+2) P s
