@@ -66,6 +66,9 @@ def _load():
     lib.oracle_ring_avg_point_f32.restype = ctypes.c_float
     lib.oracle_ring_avg_point_bf16.argtypes = [vp, i32, i64, i64]
     lib.oracle_ring_avg_point_bf16.restype = ctypes.c_uint16
+    for nm in ("oracle_ring_avg_range_f32", "oracle_ring_avg_range_bf16"):
+        getattr(lib, nm).argtypes = [vp, i32, i64, i64, i64, vp]
+        getattr(lib, nm).restype = i32
     lib.oracle_mean_f64.argtypes = [vp, i32, i64, vp]
     lib.oracle_mean_f64.restype = None
     lib.oracle_bucket_plan.argtypes = [vp, i32, i64, i64, vp, vp, i32]
@@ -196,6 +199,27 @@ def ring_avg_point_bf16(vals, p: int, i: int) -> int:
     """bf16 ring result (bit pattern) at element i, from the N bf16 inputs at i."""
     v = np.ascontiguousarray(vals, dtype=np.uint16)
     return int(_load().oracle_ring_avg_point_bf16(_ptr(v), v.shape[0], p, i))
+
+
+def ring_avg_range(rows, p: int, begin: int, out=None):
+    """Ring results at elements [begin, begin + len) of a p-element ring.
+
+    rows: the N workers' input slices at those elements (contiguous 1-D
+    float32, or uint16 bf16 bits), all of one length; out (optional): where
+    to write them.  Returns out.  Each call runs on the calling thread and
+    releases the interpreter lock, so slices can be evaluated in parallel."""
+    dt = rows[0].dtype
+    if dt not in (np.float32, np.uint16):
+        raise ValueError("rows must be float32 or bf16 bits")
+    cnt = _check_rows(rows, dt)
+    if out is None:
+        out = np.empty(cnt, dt)
+    if out.dtype != dt or out.shape != (cnt,) or not out.flags.c_contiguous:
+        raise ValueError("out must be a contiguous array of the rows' dtype and length")
+    fn = _load().oracle_ring_avg_range_f32 if dt == np.float32 else _load().oracle_ring_avg_range_bf16
+    if fn(_row_ptrs(rows), len(rows), p, begin, begin + cnt, _ptr(out)) != 0:
+        raise ValueError("ring_avg_range rejected its arguments")
+    return out
 
 
 def mean_f64(rows):

@@ -266,6 +266,80 @@ float oracle_ring_avg_point_f32(const float *vals, int n_workers, int64_t p, int
     return partial / (float)N;
 }
 
+/* The ring's result over the element range [begin, end) of a p-element ring,
+ * for comparing every output of a run too large to simulate whole at once.
+ * rows[k] points at worker k's element `begin` (the caller holds only that
+ * slice of each row); out receives end - begin results.  Every element gets
+ * what the scatter-reduce makes of it: the partial for chunk c starts as
+ * worker c's value, iteration t adds it to the value of receiver c+1+t, and
+ * the owner divides once by N ([G] "Scatter-Reduce"; the average as in
+ * oracle_ring_run_f32).  Elements do not interact, so a slice holds exactly
+ * the values the full run gives there.  The loops take one chunk at a time
+ * and, inside it, one ring iteration at a time over all its elements; each
+ * element still sees the same additions in the same order.
+ * Returns 0, or -1 on bad arguments.                                      */
+int oracle_ring_avg_range_f32(const float *const *rows, int n_workers, int64_t p, int64_t begin, int64_t end,
+                              float *out) {
+    int N = n_workers;
+    if (N < 1 || p < 0 || begin < 0 || end < begin || end > p)
+        return -1;
+    float fn = (float)N;
+    for (int c = 0; c < N; ++c) {
+        int64_t b, e;
+        oracle_chunk_range(p, N, c, &b, &e);
+        if (b < begin)
+            b = begin;
+        if (e > end)
+            e = end;
+        if (b >= e)
+            continue;
+        for (int64_t i = b; i < e; ++i)
+            out[i - begin] = rows[c][i - begin];
+        for (int t = 0; t < N - 1; ++t) {
+            const float *recv = rows[mod_n((int64_t)c + 1 + t, N)];
+            for (int64_t i = b; i < e; ++i)
+                out[i - begin] = recv[i - begin] + out[i - begin];
+        }
+        for (int64_t i = b; i < e; ++i)
+            out[i - begin] = out[i - begin] / fn;
+    }
+    return 0;
+}
+
+/* The same for bf16 rows: widened exactly, binary32 partials, the mean
+ * rounded to bf16 once (the bf16 reading above).                        */
+int oracle_ring_avg_range_bf16(const uint16_t *const *rows, int n_workers, int64_t p, int64_t begin, int64_t end,
+                               uint16_t *out) {
+    int N = n_workers;
+    if (N < 1 || p < 0 || begin < 0 || end < begin || end > p)
+        return -1;
+    float *acc = (float *)malloc((size_t)(end > begin ? end - begin : 1) * sizeof(float));
+    if (!acc)
+        return -1;
+    float fn = (float)N;
+    for (int c = 0; c < N; ++c) {
+        int64_t b, e;
+        oracle_chunk_range(p, N, c, &b, &e);
+        if (b < begin)
+            b = begin;
+        if (e > end)
+            e = end;
+        if (b >= e)
+            continue;
+        for (int64_t i = b; i < e; ++i)
+            acc[i - begin] = bf16_to_f32(rows[c][i - begin]);
+        for (int t = 0; t < N - 1; ++t) {
+            const uint16_t *recv = rows[mod_n((int64_t)c + 1 + t, N)];
+            for (int64_t i = b; i < e; ++i)
+                acc[i - begin] = bf16_to_f32(recv[i - begin]) + acc[i - begin];
+        }
+        for (int64_t i = b; i < e; ++i)
+            out[i - begin] = oracle_f32_to_bf16(acc[i - begin] / fn);
+    }
+    free(acc);
+    return 0;
+}
+
 /* The plain definition the ring reaches up to rounding order: the binary64
  * mean of the N inputs, summed in worker order.                          */
 void oracle_mean_f64(const float *const *rows, int n_workers, int64_t p, double *out) {

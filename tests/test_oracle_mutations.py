@@ -55,10 +55,26 @@ MUTANTS = [
     ("SGD step added instead of subtracted",
      "        float step = lr * avg[i];\n        w[i] = w[i] - step;",
      "        float step = lr * avg[i];\n        w[i] = w[i] + step;"),
+    ("bf16-mean SGD step added instead of subtracted",
+     "        float step = lr * bf16_to_f32(avg[i]);\n        w[i] = w[i] - step;",
+     "        float step = lr * bf16_to_f32(avg[i]);\n        w[i] = w[i] + step;"),
+    ("bf16-mean SGD as one fused multiply-add",
+     "        float step = lr * bf16_to_f32(avg[i]);\n        w[i] = w[i] - step;",
+     "        w[i] = __builtin_fmaf(-lr, bf16_to_f32(avg[i]), w[i]);"),
+    ("bf16-mean SGD step rounded to bf16",
+     "        float step = lr * bf16_to_f32(avg[i]);",
+     "        float step = bf16_to_f32(oracle_f32_to_bf16(lr * bf16_to_f32(avg[i])));"),
     ("bucket closes only above the cap",
      "if ((end - start) * elem_bytes >= cap_bytes) {", "if ((end - start) * elem_bytes > cap_bytes) {"),
     ("point evaluation folds from the wrong worker",
      "int receiver = mod_n((int64_t)c + 1 + t, N);", "int receiver = mod_n((int64_t)c + t, N);"),
+    ("range evaluation folds from the wrong worker",
+     "const float *recv = rows[mod_n((int64_t)c + 1 + t, N)];", "const float *recv = rows[mod_n((int64_t)c + t, N)];"),
+    ("bf16 range evaluation skips a worker",
+     "const uint16_t *recv = rows[mod_n((int64_t)c + 1 + t, N)];",
+     "const uint16_t *recv = rows[mod_n((int64_t)c + 2 + t, N)];"),
+    ("range evaluation multiplies with 1/N",
+     "out[i - begin] = out[i - begin] / fn;", "out[i - begin] = out[i - begin] * (1.0f / fn);"),
     ("traffic credited to the sender",
      "received[mod_n((int64_t)n + 1, N)] += e - b;", "received[n] += e - b;"),
     ("all-gather copies into the wrong chunk",

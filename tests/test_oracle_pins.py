@@ -240,6 +240,50 @@ def test_point_evaluation_matches_the_full_ring():
             assert oracle.ring_avg_point_f32(v, p, i) == rows[0][i], (n, p, i)
 
 
+def _ranges(rng, n, p):
+    """Sub-ranges of a p-element ring: whole, empty, around every chunk
+    boundary, single elements and random spans."""
+    out = [(0, p), (0, 0), (p, p)]
+    for c in range(n):
+        b, e = oracle.chunk_range(p, n, c)
+        out += [(max(0, b - 3), min(p, b + 3)), (b, e), (max(0, e - 1), e)]
+    for _ in range(12):
+        b = int(rng.integers(0, p + 1))
+        out.append((b, int(rng.integers(b, p + 1))))
+    return out
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_range_evaluation_matches_the_full_ring(bf16):
+    # The range form evaluates any slice of the ring from the input slices
+    # alone; on every slice it must give the literal simulation's bits.
+    # Rows at mixed scales make the result depend on the fold start.
+    import synth
+    rng = np.random.default_rng(41)
+    for n, p in [(1, 5), (2, 9), (3, 2), (4, 1031), (7, 100), (16, 333), (33, 40)]:
+        if bf16:
+            g = [synth.student_t3_bf16(7, k, float(rng.choice([1e-3, 1, 1e3])), 0, p) for k in range(n)]
+            rows = [r.copy() for r in g]
+            oracle.ring_allreduce_avg_bf16(rows)
+        else:
+            g = [rng.standard_normal(p).astype(np.float32) * np.float32(rng.choice([1e-3, 1, 1e3])) for _ in range(n)]
+            rows = [r.copy() for r in g]
+            oracle.ring_allreduce_avg_f32(rows)
+        whole = oracle.ring_avg_range([r.copy() for r in g], p, 0)
+        assert np.array_equal(whole.view(np.uint16 if bf16 else np.uint32), rows[0].view(np.uint16 if bf16 else np.uint32))
+        for b, e in _ranges(rng, n, p):
+            got = oracle.ring_avg_range([np.ascontiguousarray(r[b:e]) for r in g], p, b)
+            assert got.shape == (e - b,)
+            assert np.array_equal(got.view(np.uint16 if bf16 else np.uint32),
+                                  rows[0][b:e].view(np.uint16 if bf16 else np.uint32)), (n, p, b, e)
+
+
+def test_range_evaluation_rejects_a_slice_outside_the_ring():
+    g = [np.zeros(4, np.float32) for _ in range(2)]
+    with pytest.raises(ValueError):
+        oracle.ring_avg_range(g, 6, 3)  # elements 3..7 of a 6-element ring
+
+
 # --------------------------------------------------------------------------
 # invariants
 
@@ -476,6 +520,42 @@ def test_sgd_is_two_roundings_not_fma():
         if X.rn_f32(X.frac(w[i]) - X.frac(lr) * X.frac(avg[i])) != want:
             differs_from_fma += 1
     assert differs_from_fma > 0
+
+
+def test_sgd_with_bf16_gradients_uses_the_bf16_mean():
+    # bf16 gradients: every replica holds the bf16-rounded mean after the
+    # all-reduce, and that is what it applies (The Communication Problem:
+    # the averaged gradient updates the weights; DDP: every replica applies
+    # the same one).  Expected values come from the exact-rational model:
+    # the ring's binary32 fold and division, one bf16 rounding, then
+    # w - RN(lr * mean) rounded twice.  The data is chosen so that three
+    # wrong readings give other bits on some elements: updating with the
+    # binary32 mean before its bf16 rounding, a fused multiply-add, and a
+    # step lr * mean rounded to bf16.
+    import synth
+    n, p = 4, 3000
+    lr = np.float32(0.1)
+    g = [synth.student_t3_bf16(3, k, 1e-3, 0, p) for k in range(n)]
+    w = synth.normal_f32(5, 0, 0.05, 0, p)
+    rows = [r.copy() for r in g]
+    oracle.ring_allreduce_avg_bf16(rows)
+    got = w.copy()
+    oracle.sgd_update_f32(got, rows[0], lr)
+    wrong = {"binary32 mean": 0, "fma": 0, "bf16 step": 0}
+    for i in range(p):
+        c = next(k for k in range(n) if oracle.chunk_range(p, n, k)[0] <= i < oracle.chunk_range(p, n, k)[1])
+        acc = X.bf16_value(g[c][i])
+        for t in range(1, n):
+            acc = X.add(X.bf16_value(g[(c + t) % n][i]), acc)
+        m32 = X.div(acc, n)
+        m16 = X.rn_bf16(m32)
+        assert X.bf16_value(rows[0][i]) == m16
+        want = X.sub(w[i], X.mul(lr, m16))
+        assert Fraction(float(got[i])) == want, i
+        wrong["binary32 mean"] += X.sub(w[i], X.mul(lr, m32)) != want
+        wrong["fma"] += X.rn_f32(X.frac(w[i]) - X.frac(lr) * m16) != want
+        wrong["bf16 step"] += X.sub(w[i], X.rn_bf16(X.mul(lr, m16))) != want
+    assert all(v > 0 for v in wrong.values()), wrong
 
 
 # --------------------------------------------------------------------------
