@@ -22,14 +22,22 @@ def _build_host_libs():
 
 
 @pytest.fixture(autouse=True)
-def _no_out_of_bounds_access(request):
-    # Under the bounds-checked build (GRADIENT_RING_ALL_CHECKED=1) every GPU
-    # test must leave no record of a kernel touching memory outside the
-    # caller's buffers.
+def _no_device_error_record(request):
+    # After every GPU test, in the product build and in the bounds-checked
+    # build (GRADIENT_RING_ALL_CHECKED=1): no kernel left a record in the
+    # device's error word -- neither a bounded wait that gave up
+    # (RA_ERR_TIMEOUT: that block skipped its stores) nor, in the checked
+    # build, an access outside the caller's buffers (RA_ERR_BOUNDS).  Tests
+    # that cause a record on purpose read and clear it themselves.
     yield
-    if os.environ.get("GRADIENT_RING_ALL_CHECKED") != "1" or request.node.get_closest_marker("gpu") is None:
+    if request.node.get_closest_marker("gpu") is None:
         return
     import torch
+    if not torch.cuda.is_available():
+        return
     import gradient_ring_all_gb300 as ra
+    if ra._lib is None:  # the test never loaded the library
+        return
     torch.cuda.synchronize()
-    assert ra.ra_check_device_errors() != ra.RA_ERR_BOUNDS, "a kernel accessed memory outside the caller's buffers"
+    st = ra.ra_check_device_errors()
+    assert st == ra.RA_OK, "a kernel left a device error record: %s" % ra.ra_status_str(st)

@@ -2,6 +2,8 @@
 the layouts the tests need, and read sampled outputs back."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -79,3 +81,63 @@ def fill_device_rows(wl, rows, chunk_elems=1 << 26):
 def gather(rows, idx):
     it = torch.from_numpy(idx).to("cuda")
     return [to_host(r.index_select(0, it)) for r in rows]
+
+
+def fill_and_expect(wl, rows, rings=None, slice_elems=1 << 24, sub_elems=1 << 15, threads=None):
+    """Put the workload's inputs in `rows` and compute the ring's result for
+    every element on the host.
+
+    The rows are generated slice by slice into a host buffer; each slice is
+    copied to the device rows (tensors of any placement) and, from the same
+    host bytes, the oracle's range evaluation gives the ring's result for
+    every element of the slice.  rings: [(offset, count)] element ranges
+    that are rings of their own (the buckets), or None for one ring over all
+    p elements.  Returns the expected result, p elements (float32, or uint16
+    bf16 bits).  The oracle's calls run on a thread pool (they release the
+    interpreter lock), one sub-slice each."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    n, p = wl.n, wl.p
+    bf16 = wl.dtype == "bf16"
+    hdt = np.uint16 if bf16 else np.float32
+    s_el = min(slice_elems, max(1, p))
+    host = torch.empty((n, s_el), dtype=torch.int16 if bf16 else torch.float32).pin_memory()
+    hnp = host.numpy().view(hdt)
+    expected = np.empty(p, hdt)
+    rings = [(0, p)] if rings is None else list(rings)
+    threads = threads or max(1, min(32, os.cpu_count() or 1))
+    with ThreadPoolExecutor(threads) as ex:
+        for off, cnt in rings:
+            for s in range(0, cnt, s_el):
+                c = min(s_el, cnt - s)
+                for k in range(n):
+                    wl.fill_row(host[k].data_ptr(), k, off + s, c)
+                    src = host[k, :c].view(torch.bfloat16) if bf16 else host[k, :c]
+                    rows[k][off + s:off + s + c].copy_(src, non_blocking=True)
+
+                def part(a, s=s, c=c, off=off, cnt=cnt):
+                    b = min(c, a + sub_elems)
+                    oracle.ring_avg_range([hnp[k, a:b] for k in range(n)], cnt, s + a,
+                                          out=expected[off + s + a:off + s + b])
+
+                list(ex.map(part, range(0, c, sub_elems)))
+                torch.cuda.current_stream().synchronize()  # the copies are done with the host slice
+    del host
+    return expected
+
+
+def assert_row_equals(row, expected, begin=0, end=None, what="", slice_elems=1 << 26):
+    """Every element of the device row [begin, end) equals `expected`
+    [begin, end) bit for bit (read back in slices)."""
+    end = expected.shape[0] if end is None else end
+    bits = np.uint16 if expected.dtype == np.uint16 else np.uint32
+    for s in range(begin, end, slice_elems):
+        e = min(end, s + slice_elems)
+        got = to_host(row[s:e]).view(bits)
+        want = expected[s:e].view(bits)
+        if not np.array_equal(got, want):
+            bad = np.flatnonzero(got != want)
+            raise AssertionError("%s: %d of %d elements differ from the oracle, first at %d (got %#x, want %#x)"
+                                 % (what, bad.size, e - s, s + int(bad[0]), int(got[bad[0]]), int(want[bad[0]])))
