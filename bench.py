@@ -286,7 +286,208 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# inputs, and the check of what a call produced
+
+
+def fill_workload(wl, rows, w=None, rings=None, verify=False, slice_elems=1 << 24, sub_elems=1 << 15):
+    """Generate the workload's rows (and its SGD weights) on the host, slice
+    by slice, and copy them to the device tensors `rows` (and `w`).
+
+    With `verify`, the CPU oracle's range evaluation runs on the same host
+    slices, so the result of the workload's call is known for every element:
+    returns (mean row, weights after the SGD step or None) as host arrays
+    (float32, or uint16 bf16 bits).  Without it, returns (None, None).
+    rings: [(offset, count)] element ranges reduced as rings of their own
+    (the buckets), or None for one ring of all p elements.  The oracle only
+    reads the host copies of the inputs: it checks the GPU's result and is
+    never on the path that produces it."""
+    import numpy as np
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+    n, p = wl.n, wl.p
+    bf16 = wl.dtype == "bf16"
+    hdt = np.uint16 if bf16 else np.float32
+    s_el = min(slice_elems, max(1, p))
+    host = torch.empty((n, s_el), dtype=torch.int16 if bf16 else torch.float32).pin_memory()
+    hnp = host.numpy().view(hdt)
+    hw = torch.empty(s_el, dtype=torch.float32).pin_memory() if w is not None else None
+    mean = wexp = None
+    if verify:
+        import oracle
+        mean = np.empty(p, hdt)
+        wexp = np.empty(p, np.float32) if w is not None else None
+    stream = torch.cuda.current_stream()
+    with ThreadPoolExecutor(max(1, min(32, os.cpu_count() or 1))) as ex:
+        for off, cnt in ([(0, p)] if rings is None else rings):
+            for s in range(0, cnt, s_el):
+                c, g = min(s_el, cnt - s), off + s
+                for k in range(n):
+                    wl.fill_row(host[k].data_ptr(), k, g, c)
+                    rows[k][g:g + c].copy_(host[k, :c].view(torch.bfloat16) if bf16 else host[k, :c],
+                                           non_blocking=True)
+                if w is not None:
+                    wl.fill_weights(hw.data_ptr(), g, c)
+                    w[g:g + c].copy_(hw[:c], non_blocking=True)
+                if verify:
+                    def part(a, s=s, c=c, g=g, cnt=cnt):
+                        b = min(c, a + sub_elems)
+                        oracle.ring_avg_range([hnp[k, a:b] for k in range(n)], cnt, s + a, out=mean[g + a:g + b])
+                        if wexp is not None:
+                            wexp[g + a:g + b] = hw.numpy()[a:b]
+                            oracle.sgd_update_f32(wexp[g + a:g + b], mean[g + a:g + b], wl.sgd_lr)
+
+                    list(ex.map(part, range(0, c, sub_elems)))
+                stream.synchronize()  # the copies are done with the host slice
+    return mean, wexp
+
+
+def _bits(a):
+    """Integer view of a host array of float32 or bf16 bits, for bitwise comparison."""
+    import numpy as np
+    return a.view(np.uint16) if a.dtype == np.uint16 else a.view(np.uint32)
+
+
+def _host_bits(t):
+    """A device tensor's values as host integers (bf16 -> uint16, float32 -> uint32)."""
+    import numpy as np
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy().view(np.uint32)
+
+
+def check_result(rows, mean, w=None, wexp=None, slice_elems=1 << 26):
+    """Compare a call's result with the oracle's on every element: worker
+    0's row read back whole against `mean`, every other worker's row against
+    worker 0's on the device, and the SGD weights against `wexp`.  Returns
+    {"bit_exact": bool, "first_mismatch": None or where}."""
+    import numpy as np
+    import torch
+
+    def first_diff(dev, want):
+        for s in range(0, want.shape[0], slice_elems):
+            e = min(want.shape[0], s + slice_elems)
+            d = np.flatnonzero(_host_bits(dev[s:e]) != _bits(want[s:e]))
+            if d.size:
+                return s + int(d[0])
+        return None
+
+    i = first_diff(rows[0], mean)
+    if i is not None:
+        return {"bit_exact": False, "first_mismatch": "worker 0, element %d" % i}
+    iv = torch.int16 if rows[0].dtype == torch.bfloat16 else torch.int32
+    for k, r in enumerate(rows[1:], 1):
+        if not torch.equal(rows[0].view(iv), r.view(iv)):
+            return {"bit_exact": False, "first_mismatch": "worker %d differs from worker 0" % k}
+    if wexp is not None:
+        i = first_diff(w, wexp)
+        if i is not None:
+            return {"bit_exact": False, "first_mismatch": "weights, element %d" % i}
+    return {"bit_exact": True, "first_mismatch": None}
+
+
+def error_vs_binary64(wl, mean, count=200_000, seed=11):
+    """The binary32 ring mean against the binary64 mean of the inputs, on
+    `count` random elements (regenerated from the seeded generator): the
+    norm-relative error, and the largest element error in units of the mean
+    absolute input (the recursive-summation bound makes that (N-1)u at
+    most; the stated tolerance is 1e-5)."""
+    import numpy as np
+    idx = np.unique(np.random.default_rng(seed).integers(0, wl.p, count)).astype(np.int64)
+    vals = np.stack([wl.values_at(k, idx).astype(np.float64) for k in range(wl.n)])
+    m64 = vals.mean(axis=0)
+    err = mean[idx].astype(np.float64) - m64
+    return {"norm": float(np.linalg.norm(err) / np.linalg.norm(m64)),
+            "max_elementwise": float(np.max(np.abs(err) / np.abs(vals).mean(axis=0))),
+            "sample": "%d random elements" % idx.size}
+
+
+def _time_steps(step, steps, stream, dist=None):
+    """CUDA events around each call on the launch stream, inside the
+    barrier-bracketed timed region; returns (total ms max over ranks, mean
+    ms per call)."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+
+    def one(k):
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+
+    _, total_ms = timed_region(one, steps, dist, _CudaEventTimer(stream))
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return total_ms, sum(per) / len(per)
+
+
+# the other configurations of the benchmark, each measured the way the
+# headline is: inputs filled from the seeded generator, the first call
+# compared with the oracle on every element, then timed
+PER_CONFIG = (("ring4_uneven_1m_f32", "allreduce"), ("transformer24_buckets_n4_f32", "buckets"),
+              ("transformer24_buckets_n4_f32", "buckets_each"), ("student_t3_1g_n16_bf16", "allreduce"),
+              ("resnet18_sgd_n32_f32", "sgd"))
+
+
+def measure_config(ra, wl, calls, steps, warmup, peak):
+    """One workload, one or more calls on it: verified first call, then
+    `warmup` more and `steps` timed.  Returns one result dict per call."""
+    import torch
+    stream = torch.cuda.current_stream()
+    bf16 = wl.dtype == "bf16"
+    esz = 2 if bf16 else 4
+    rows = [torch.empty(wl.p, dtype=torch.bfloat16 if bf16 else torch.float32, device="cuda") for _ in range(wl.n)]
+    w = torch.empty(wl.p, dtype=torch.float32, device="cuda") if wl.sgd_lr > 0 else None
+    plan = ra.ra_bucket_plan(wl.tensors, esz, wl.bucket_cap_bytes) if wl.bucket_cap_bytes else None
+    mean, wexp = fill_workload(wl, rows, w, rings=plan, verify=True)
+    # every call starts from the same inputs: a device copy to restore them
+    keep = [r.clone() for r in rows] + ([w.clone()] if w is not None else []) if len(calls) > 1 else None
+    out = []
+    for j, call in enumerate(calls):
+        if j > 0:
+            for r, k in zip(rows + ([w] if w is not None else []), keep):
+                r.copy_(k)
+        if call == "allreduce":
+            step = lambda: ra.ra_allreduce_avg(rows, stream)
+        elif call == "sgd":
+            step = lambda: ra.ra_allreduce_sgd(rows, w, wl.sgd_lr, stream)
+        elif call == "buckets":
+            step = lambda: ra.ra_allreduce_avg_buckets(rows, plan, stream)
+        else:  # buckets_each: one call, and so one launch, per bucket, output side first
+            def step():
+                for b in plan:
+                    ra.ra_allreduce_avg_buckets(rows, [b], stream)
+        step()
+        torch.cuda.synchronize()
+        chk = check_result(rows, mean, w, wexp)
+        for _ in range(warmup - 1):
+            step()
+        _, ms = _time_steps(step, steps, stream)
+        torch.cuda.synchronize()
+        st = ra.ra_check_device_errors()
+        nbytes = call_bytes(call, wl.n, wl.p, esz)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res = {"workload": wl.name, "call": call, "workers": wl.n, "elements_per_worker": wl.p, "dtype": wl.dtype,
+               "bytes_per_call": nbytes, "ms_per_call": ms, "gbs": gbs, "frac": gbs / peak,
+               "pct_of_nominal_hbm": 100.0 * gbs / NOMINAL_HBM_GBS, "steps": steps,
+               "bit_exact": chk["bit_exact"] and st == ra.RA_OK,
+               "device_errors": ra.ra_status_str(st)}
+        if chk["first_mismatch"]:
+            res["first_mismatch"] = chk["first_mismatch"]
+        if plan:
+            res["buckets"] = len(plan)
+            res["launches_per_call"] = len(plan) if call == "buckets_each" else 1
+        if wl.n * wl.p * esz < 129e6:
+            res["note"] = "inputs of %.1f MB fit the 129 MB L2; the call is launch-bound" % (wl.n * wl.p * esz / 1e6)
+        out.append(res)
+    del rows, w, keep
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
+    import dataclasses
+
     import torch
     ws, rank, local = _dist()
     if args.gpus > 1 and ws == 1:
@@ -302,55 +503,55 @@ def run_ours(args):
     import synth
     ra.load()
     wl = synth.WORKLOADS[WORKLOAD]
-    n, p = wl.n, (args.elements or wl.p)
+    if args.elements:
+        wl = dataclasses.replace(wl, p=args.elements)
+    n, p = wl.n, wl.p
     nbytes = 2 * n * p * 4  # every input read once, the mean written to every worker once
+    verify = args.legs == "all"
 
-    # inputs: each worker's row generated on the host, copied to its own allocation
+    # inputs: each worker's row generated on the host, copied to its own
+    # allocation; the oracle's result for every element computed beside it
     rows = [torch.empty(p, dtype=torch.float32, device="cuda") for _ in range(n)]
-    piece = 1 << 26
-    host = torch.empty(piece, dtype=torch.float32).pin_memory()
-    for k in range(n):
-        for s in range(0, p, piece):
-            c = min(piece, p - s)
-            wl.fill_row(host.data_ptr(), k, s, c)
-            rows[k][s:s + c].copy_(host[:c])
-    del host
+    mean, _ = fill_workload(wl, rows, verify=verify)
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    # the first warm-up call runs on the fresh inputs: its result is compared
+    # with the oracle's on every element (the timed calls then re-average
+    # rows that are already identical, which moves the same bytes)
+    ra.ra_allreduce_avg(rows, stream)
+    torch.cuda.synchronize()
+    check = check_result(rows, mean) if verify else None
+    err64 = error_vs_binary64(wl, mean) if verify and check["bit_exact"] else None
+    del mean
+    for _ in range(args.warmup - 1):
         ra.ra_allreduce_avg(rows, stream)
     torch.cuda.synchronize()
 
     # timed region: K launches, an event pair around each on the launch stream
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = _ClockSampler(local).start()
     time.sleep(0.3)
-
-    def step(k):
-        starts[k].record(stream)
-        ra.ra_allreduce_avg(rows, stream)
-        ends[k].record(stream)
-
     w0 = time.time()
-    _, total_ms = timed_region(step, args.steps, dist, _CudaEventTimer(stream))
+    total_ms, avg_kernel_ms = _time_steps(lambda: ra.ra_allreduce_avg(rows, stream), args.steps, stream, dist)
     w1 = time.time()
     clk = clocks.stop(w0, w1)
-    kern_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # a bounded wait that gave up inside the timed region would have skipped
+    # its block's stores: the device's error word must be clean
+    torch.cuda.synchronize()
+    dev_status = ra.ra_check_device_errors()
     ms_per_step = total_ms / args.steps
     value = aggregate_gbs(nbytes, ws, ms_per_step)
-    avg_kernel_ms = sum(kern_ms) / len(kern_ms)
 
     if args.legs == "device":
         # profiling runs (e.g. a smaller --elements under ncu): device loop only
         if rank == 0:
             print(json.dumps({"profile_run": True, "workload": WORKLOAD, "workers": n, "elements_per_worker": p,
                               "ms_per_step": total_ms / args.steps,
-                              "gbs": nbytes / (total_ms / args.steps / 1e3) / 1e9}), flush=True)
+                              "gbs": nbytes / (total_ms / args.steps / 1e3) / 1e9,
+                              "device_errors": ra.ra_status_str(dev_status)}), flush=True)
         if dist:
             dist.destroy_process_group()
-        return 0
+        return 0 if dev_status == ra.RA_OK else 3
 
     # end to end through the host-buffer entry point: every step the fused
     # kernel reads the 8 pinned host rows and writes the mean back to all of
@@ -370,12 +571,28 @@ def run_ours(args):
     e2e_ms = time_host(ra.RA_HOST_DIRECT, e2e_steps)
     staged_ms = time_host(ra.RA_HOST_STAGED, max(1, e2e_steps // 2))
     del hrows
-
-    if rank != 0:
-        dist.destroy_process_group()
-        return 0
+    torch.cuda.synchronize()
+    host_status = ra.ra_check_device_errors()
+    del rows
+    torch.cuda.empty_cache()
 
     peak, peak_kind = _peaks()
+    per_config = None
+    if ws == 1 and not args.elements and args.per_config:
+        per_config = []
+        done = {}
+        for name, call in PER_CONFIG:
+            done.setdefault(name, []).append(call)
+        for name, calls in done.items():
+            per_config += measure_config(ra, synth.WORKLOADS[name], calls, args.config_steps, 3, peak)
+
+    # every replica verified its own first call and timed region
+    mine = bool(check and check["bit_exact"]) and dev_status == ra.RA_OK and host_status == ra.RA_OK
+    bit_exact = max_over_ranks(0.0 if mine else 1.0, dist) == 0.0
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0 if mine or not verify else 3
+
     achieved = nbytes / (avg_kernel_ms / 1e3) / 1e9
     cpu_gbs, cpu_s, reps = None, None, 16
     if ws == 1:
@@ -385,6 +602,13 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": _config(wl, n, p, ws),
+        "bit_exact": bit_exact,
+        "max_rel_err_vs_f64": err64,
+        "verification": {"first_call": "every element of worker 0's row against the CPU oracle's ring over the same "
+                                       "inputs; every other worker's row against worker 0's",
+                         "first_mismatch": check and check["first_mismatch"],
+                         "device_errors_after_timed_region": ra.ra_status_str(dev_status),
+                         "device_errors_after_e2e": ra.ra_status_str(host_status)},
         "pct_of_measured_hbm": 100.0 * value / ws / peak,
         "pct_of_nominal_hbm": 100.0 * value / ws / NOMINAL_HBM_GBS,
         "elements_per_s": n * p * ws / (ms_per_step / 1e3),
@@ -402,6 +626,8 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "clocks": clk,
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     if args.elements:
         line["config"]["note"] = "reduced --elements: not the benchmark configuration"
     if cpu_gbs is not None:
@@ -412,11 +638,12 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
-    return 0
+    ok = bit_exact and all(c["bit_exact"] for c in (per_config or []))
+    return 0 if ok or not verify else 3
 
 
 CALLS = ("allreduce", "staged", "sgd", "buckets", "buckets_each", "reduce_scatter", "all_gather", "single_reducer",
-         "bf16_wire", "host")
+         "bf16_wire", "host", "host_link")
 
 
 def call_bytes(call: str, n: int, p: int, esz: int) -> int:
@@ -511,6 +738,85 @@ def run_profile_call(args):
     return 0
 
 
+def run_host_link(args):
+    """What the host link delivers, as the ceiling of the end-to-end number:
+    N rows of P fp32 in pinned host memory (the bench workload's shape),
+    moved by the copy engines (one cudaMemcpyAsync per row: host to device,
+    device to host, and both at once on two streams) and by this library's
+    kernels working on the host rows directly over NVLink-C2C (the
+    reduce-scatter reads N*P and writes P elements, the all-gather reads P
+    and writes (N-1)*P, the all-reduce reads and writes N*P).  One JSON line,
+    GB/s of host-side bytes for each."""
+    import ctypes
+
+    import torch
+    from gradient_ring_all_gb300 import build
+    build.build()
+    import gradient_ring_all_gb300 as ra
+    import synth
+    lib = ra.load()
+    wl = synth.WORKLOADS[args.workload]
+    n, p = (args.workers or wl.n), (args.elements or wl.p)
+    esz = 2 if wl.dtype == "bf16" else 4
+    dt = torch.bfloat16 if esz == 2 else torch.float32
+    code = ra.RA_BF16 if esz == 2 else ra.RA_F32
+    h = [torch.zeros(p, dtype=dt).pin_memory() for _ in range(n)]
+    d = [torch.empty(p, dtype=dt, device="cuda") for _ in range(n)]
+    s0 = torch.cuda.current_stream()
+    s1 = torch.cuda.Stream()
+    arr = (ctypes.c_void_p * n)(*[x.data_ptr() for x in h])  # pinned host memory is device-addressable
+    st = ctypes.c_void_p(s0.cuda_stream)
+
+    def h2d():
+        for a, b in zip(d, h):
+            a.copy_(b, non_blocking=True)
+
+    def d2h():
+        for a, b in zip(h, d):
+            a.copy_(b, non_blocking=True)
+
+    def both():
+        half = n // 2
+        for a, b in zip(d[:half], h[:half]):
+            a.copy_(b, non_blocking=True)
+        s1.wait_stream(s0)
+        with torch.cuda.stream(s1):
+            for a, b in zip(h[half:], d[half:]):
+                a.copy_(b, non_blocking=True)
+        s0.wait_stream(s1)
+
+    def call(fn, what):
+        def run():
+            rc = fn()
+            if rc != 0:
+                raise RuntimeError("%s: %s" % (what, ra.ra_status_str(rc)))
+        return run
+
+    legs = [
+        ("copy_h2d", h2d, n * p * esz),
+        ("copy_d2h", d2h, n * p * esz),
+        ("copy_h2d_and_d2h_concurrent", both, n * p * esz),
+        ("kernel_reduce_scatter_on_host_rows", call(lambda: lib.ra_reduce_scatter_avg(arr, n, p, code, None, st),
+                                                    "ra_reduce_scatter_avg"), (n + 1) * p * esz),
+        ("kernel_all_gather_on_host_rows", call(lambda: lib.ra_all_gather(arr, n, p, code, None, st),
+                                                "ra_all_gather"), n * p * esz),
+        ("kernel_allreduce_on_host_rows", call(lambda: lib.ra_allreduce_avg(arr, n, p, code, st), "ra_allreduce_avg"),
+         2 * n * p * esz),
+    ]
+    out = {"profile_run": True, "call": "host_link", "workload": args.workload, "workers": n,
+           "elements_per_worker": p, "host_memory": "pinned (cudaHostAlloc through torch)"}
+    steps = max(1, min(args.steps, 10))
+    for name, fn, nbytes in legs:
+        fn()
+        _, ms = timed_region(lambda k: fn(), steps, None, _CudaEventTimer(s0))
+        ms /= steps
+        out[name] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9}
+    torch.cuda.synchronize()
+    out["device_errors"] = ra.ra_status_str(ra.ra_check_device_errors())
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_overlap(args):
     """Overlap of the bucketed all-reduce with a synthetic backward pass
     (Gibiansky, "Applying the Allreduce to Deep Learning").  The backward of
@@ -593,6 +899,9 @@ def main(argv=None):
                     help="--call: worker count instead of the workload's (with --elements for the length)")
     ap.add_argument("--layout", choices=["separate", "strided"], default="separate",
                     help="--call: one allocation per worker, or rows back to back with stride P+1 elements")
+    ap.add_argument("--per-config", dest="per_config", action=argparse.BooleanOptionalAction, default=True,
+                    help="after the headline (N=1, full size): also measure and verify every other configuration")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed calls per configuration in per_config")
     ap.add_argument("--overlap", action="store_true",
                     help="experiment: bucketed all-reduce overlapped with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=8192, help="--overlap: tokens per backward step")
@@ -603,6 +912,8 @@ def main(argv=None):
         return run_reference(args)
     if args.overlap:
         return run_overlap(args)
+    if args.call == "host_link":
+        return run_host_link(args)
     if args.call:
         return run_profile_call(args)
     return run_ours(args)

@@ -1,6 +1,8 @@
 """bench.py's JSON line on the GPU: a reduced run (20M elements per worker)
 must print one line with every key of the benchmark contract, consistent
-values, and the roofline and CPU-baseline objects."""
+values, the roofline and CPU-baseline objects, and the check of what it
+timed (bit-exact first call, clean device error word).  The host-link leg
+prints its copy-engine and kernel figures."""
 from __future__ import annotations
 
 import json
@@ -45,3 +47,17 @@ def test_bench_line_has_the_contract_keys():
     assert c["kind"] == "oracle" and c["cores"] >= 1 and c["value"] > 0 and c["sample"]
     assert d["gpu_launches"] == 5
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    assert d["bit_exact"] is True
+    v = d["verification"]
+    assert v["first_mismatch"] is None and v["device_errors_after_timed_region"] == "RA_OK"
+    m = d["max_rel_err_vs_f64"]
+    assert 0 <= m["norm"] <= 1e-5 and 0 <= m["max_elementwise"] <= 1e-5
+    assert "per_config" not in d  # reduced runs measure the headline only
+
+
+def test_host_link_leg():
+    d = _line("--call", "host_link", "--elements", "4000000", "--steps", "2", "--warmup", "3")
+    for k in ("copy_h2d", "copy_d2h", "copy_h2d_and_d2h_concurrent", "kernel_reduce_scatter_on_host_rows",
+              "kernel_all_gather_on_host_rows", "kernel_allreduce_on_host_rows"):
+        assert d[k]["gbs"] > 0 and d[k]["bytes"] > 0, k
+    assert d["device_errors"] == "RA_OK"
