@@ -26,6 +26,10 @@
  *   - the SGD variant computes w - (lr * avg) with two roundings.
  *
  * Conventions shared by every call:
+ *   - `dtype` is an int holding an ra_dtype value and `stream` a void *
+ *     holding a cudaStream_t, so that this header needs no CUDA header and
+ *     compiles as plain C; the values are those of the enum and the
+ *     runtime's stream handle.
  *   - `bufs` is a HOST array of n DEVICE pointers, one per worker; each
  *     points at p elements of `dtype`, element-aligned.  The array itself
  *     is read during the call only.  The buffers must not overlap.
@@ -164,7 +168,8 @@ ra_status ra_bucket_plan(const int64_t *numel, int ntensors, int elem_bytes, int
 /*
  * ra_allreduce_avg_buckets -- every bucket of every worker's array is
  * all-reduced-averaged as a ring of its own (its own P = count and its own
- * N chunks).  The (bucket, chunk) pieces go to the fused kernel in as few
+ * N chunks): the all-reduce run on a subset of the parameters at a time
+ * (Gibiansky, "Applying the Allreduce to Deep Learning").  The (bucket, chunk) pieces go to the fused kernel in as few
  * launches as the kernel-parameter space allows (at most 896 pieces per
  * launch); the result does not depend on that split.
  *   bufs   host array of n device pointers; each buffer must hold every
@@ -364,7 +369,11 @@ ra_status ra_selftest_bounds_check(void *const *bufs, int n, int64_t p, int dtyp
 ra_status ra_selftest_wait_timeout(int timeout_us, void *stream);
 
 /* ra_chunk_range -- [begin, end) of chunk c of a p-element array split for
- * n workers (the first p mod n chunks hold one extra element). */
+ * n workers.  Gibiansky, "Scatter-Reduce", divides the array into N chunks
+ * but leaves open how the split goes when N does not divide P; this
+ * library's reading, used by every call, gives the first p mod n chunks one
+ * extra element: chunk c = [c*q + min(c,r), (c+1)*q + min(c+1,r)) with
+ * q = p / n, r = p mod n.  0 <= c < n; nothing is checked. */
 void ra_chunk_range(int64_t p, int n, int c, int64_t *begin, int64_t *end);
 
 /* ra_status_str -- a static, human-readable name for a status. */
