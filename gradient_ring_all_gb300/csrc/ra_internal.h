@@ -154,6 +154,8 @@ __host__ __device__ inline void unaligned_interior(int64_t b, int64_t e, int V, 
 // (room for the widening), a weight slot for SGD, the mbarrier, the per-row
 // byte offsets and staging offsets, and (8-byte aligned) the rows' tile
 // pointers
+// n row slots | weight slot (SGD) | mbarrier | shift[n + 1], ringoff[n] |
+// (8-byte alignment) rowptr[n]
 inline size_t unaligned_smem_bytes(int n, int tile_bytes, int out, int esz) {
     return (size_t)n * ((size_t)tile_bytes + 16) + (out == kOutAllSgd ? (size_t)(tile_bytes / esz) * 4 + 16 : 0) + 16 +
            (size_t)(2 * n + 1) * sizeof(int) + 8 + (size_t)n * sizeof(char *);

@@ -495,8 +495,88 @@ __device__ __forceinline__ void put_elem(void *p, T v) {
 // with packed rows: 2 for the all-reduce (bf16 N=16: 6.47 TB/s, against 5.82
 // with 1 and 5.87 with 4; binary32 within 1 %), 4 for the reduce-scatter
 // (7.35 against 7.11 TB/s with 2).
+#ifndef RA_UNALIGNED_J
+#define RA_UNALIGNED_J 0
+#endif
 template <int OUT>
-constexpr int unaligned_per_thread() { return OUT == kOutOne ? 4 : 2; }
+constexpr int unaligned_per_thread() { return RA_UNALIGNED_J > 0 ? RA_UNALIGNED_J : (OUT == kOutOne ? 4 : 2); }
+
+// One pass of the unaligned kernel over elements j0 + u * kThreads (u < J)
+// of the staged tile.  ringoff[t] is where row (c + t) mod n's elements
+// start in shared memory, so the fold is one loop in ring order; rowptr[k]
+// is row k's first element of the tile in global memory.  In a FULL pass
+// every element exists (no bounds checks); the tile's last pass checks
+// each against ne.
+template <class E, int OUT, int J, bool FULL, int MAXSEG>
+__device__ __forceinline__ void unaligned_pass(const FusedParams<MAXSEG> &p, const unsigned char *smem,
+                                               const int *ringoff, char *const *rowptr, const int *shift,
+                                               unsigned char *wslot, int n, int c, int ne, int64_t first, int j0) {
+    using T = typename E::T;
+    constexpr int esz = (int)sizeof(T);
+    constexpr int step = kThreads * esz;  // bytes between one thread's elements
+    const int boff = j0 * esz;
+    bool in[J];
+#pragma unroll
+    for (int u = 0; u < J; ++u) in[u] = FULL || j0 + u * kThreads < ne;
+    float acc[J];
+    {
+        const unsigned char *b = smem + ringoff[0] + boff;
+#pragma unroll
+        for (int u = 0; u < J; ++u) acc[u] = in[u] ? ld_staged<T>(b + u * step) : 0.f;
+    }
+#pragma unroll 4
+    for (int t = 1; t < n; ++t) {
+        const unsigned char *b = smem + ringoff[t] + boff;
+#pragma unroll
+        for (int u = 0; u < J; ++u)
+            if (in[u]) {
+                acc[u] = __fadd_rn(ld_staged<T>(b + u * step), acc[u]);
+                if constexpr (OUT == kOutAllWire) acc[u] = round_bf16(acc[u]);
+            }
+    }
+    T v[J];
+    float held[J];
+#pragma unroll
+    for (int u = 0; u < J; ++u) {
+        const float avg = div_n(acc[u], n);
+        if constexpr (esz == 4) {
+            v[u] = avg;
+            held[u] = avg;
+        } else {
+            v[u] = (T)f32_to_bf16_bits(avg);
+            held[u] = bf16_bits_to_f32(v[u]);
+        }
+    }
+    if constexpr (OUT == kOutOne) {
+        char *bp = reinterpret_cast<char *>(p.aux[c]) + first * esz + boff;
+#pragma unroll
+        for (int u = 0; u < J; ++u)
+            if (in[u]) put_elem<T>(bp + u * step, v[u]);
+    } else {
+        for (int k = 0; k < n; ++k) {
+            char *bp = rowptr[k] + boff;
+#pragma unroll
+            for (int u = 0; u < J; ++u)
+                if (in[u]) put_elem<T>(bp + u * step, v[u]);
+        }
+        if constexpr (OUT == kOutAllSgd) {
+            // whole granules of the weights go back by bulk copy, the
+            // partial ones at the tile's ends element by element
+            const int d = shift[n], lo = (d + 15) & ~15, hi = (d + ne * 4) & ~15;
+#pragma unroll
+            for (int u = 0; u < J; ++u) {
+                const int j = j0 + u * kThreads;
+                if (in[u]) {
+                    const int pos = d + j * 4;
+                    float *wp = reinterpret_cast<float *>(wslot + pos);
+                    const float nw = __fsub_rn(*wp, __fmul_rn(p.lr, held[u]));
+                    if (pos >= lo && pos < hi) *wp = nw;
+                    else __stcs(p.w + first + j, nw);
+                }
+            }
+        }
+    }
+}
 
 template <class E, int OUT, int MAXSEG>
 __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __grid_constant__ TmaFusedParams<MAXSEG> tp) {
@@ -514,13 +594,13 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
     const int wslot_bytes = OUT == kOutAllSgd ? (B / esz) * 4 + 16 : 0;
     uint64_t *bar = reinterpret_cast<uint64_t *>(wslot + wslot_bytes);
     int *shift = reinterpret_cast<int *>(wslot + wslot_bytes + 16);  // d_k of row k; shift[n]: the weights'
-    // per tile: where row k's elements start in shared memory, and row k's
-    // first element of the tile in global memory (set by thread 0, so that
-    // the fold and the stores do no per-row address arithmetic: measured
-    // +2.5 % for bf16 at n=16, +0.2-0.3 % in binary32)
-    int *rowoff = shift + n + 1;
+    // per tile (set by thread 0, so that the fold and the stores do no
+    // per-row address arithmetic): ringoff[t], where row (c + t) mod n's
+    // elements start in shared memory, in the fold's ring order; rowptr[k],
+    // row k's first element of the tile in global memory
+    int *ringoff = shift + n + 1;
     char **rowptr = reinterpret_cast<char **>(
-        (reinterpret_cast<uintptr_t>(rowoff + n) + 7) & ~static_cast<uintptr_t>(7));
+        (reinterpret_cast<uintptr_t>(ringoff + n) + 7) & ~static_cast<uintptr_t>(7));
     pdl_enter();
 
     for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
@@ -569,7 +649,7 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
                 for (int k = 0; k < n; ++k) {
                     const int d = (int)((reinterpret_cast<uintptr_t>(p.rows[k]) + (uintptr_t)first * esz) & 15);
                     shift[k] = d;
-                    rowoff[k] = k * slot + d;
+                    ringoff[k >= c ? k - c : k + n - c] = k * slot + d;
                     rowptr[k] = reinterpret_cast<char *>(p.rows[k]) + first * esz;
                     total += (uint32_t)((d + bytes + 15) & ~15);
                 }
@@ -607,73 +687,15 @@ __global__ void __launch_bounds__(kThreads) fused_tma_unaligned_kernel(const __g
                 __syncthreads();
                 return;
             }
-            for (int j0 = threadIdx.x; j0 < ne; j0 += J * kThreads) {
-                float acc[J];
-                auto add_row = [&](int r) {
-                    const unsigned char *b = smem + rowoff[r];
-#pragma unroll
-                    for (int u = 0; u < J; ++u) {
-                        const int j = j0 + u * kThreads;
-                        if (j < ne) {
-                            acc[u] = __fadd_rn(ld_staged<T>(b + j * esz), acc[u]);
-                            if constexpr (OUT == kOutAllWire) acc[u] = round_bf16(acc[u]);
-                        }
-                    }
-                };
-                {
-                    const unsigned char *b = smem + rowoff[c];
-#pragma unroll
-                    for (int u = 0; u < J; ++u) {
-                        const int j = j0 + u * kThreads;
-                        acc[u] = j < ne ? ld_staged<T>(b + j * esz) : 0.f;
-                    }
-                }
-                // ring order from row c: c + 1 .. n - 1, then 0 .. c - 1
-                for (int r = c + 1; r < n; ++r) add_row(r);
-                for (int r = 0; r < c; ++r) add_row(r);
-                T v[J];
-                float held[J];
-#pragma unroll
-                for (int u = 0; u < J; ++u) {
-                    const float avg = div_n(acc[u], n);
-                    if constexpr (esz == 4) {
-                        v[u] = avg;
-                        held[u] = avg;
-                    } else {
-                        v[u] = (T)f32_to_bf16_bits(avg);
-                        held[u] = bf16_bits_to_f32(v[u]);
-                    }
-                }
-                if constexpr (OUT == kOutOne) {
-                    char *base = reinterpret_cast<char *>(p.aux[c]) + first * esz;
-#pragma unroll
-                    for (int u = 0; u < J; ++u)
-                        if (j0 + u * kThreads < ne) put_elem<T>(base + (j0 + u * kThreads) * esz, v[u]);
-                } else {
-                    for (int k = 0; k < n; ++k) {
-                        char *base = rowptr[k];
-#pragma unroll
-                        for (int u = 0; u < J; ++u)
-                            if (j0 + u * kThreads < ne) put_elem<T>(base + (j0 + u * kThreads) * esz, v[u]);
-                    }
-                    if constexpr (OUT == kOutAllSgd) {
-                        // whole granules of the weights go back by bulk copy, the
-                        // partial ones at the tile's ends element by element
-                        const int d = shift[n], lo = (d + 15) & ~15, hi = (d + ne * 4) & ~15;
-#pragma unroll
-                        for (int u = 0; u < J; ++u) {
-                            const int j = j0 + u * kThreads;
-                            if (j < ne) {
-                                const int pos = d + j * 4;
-                                float *wp = reinterpret_cast<float *>(wslot + pos);
-                                const float nw = __fsub_rn(*wp, __fmul_rn(p.lr, held[u]));
-                                if (pos >= lo && pos < hi) *wp = nw;
-                                else __stcs(p.w + first + j, nw);
-                            }
-                        }
-                    }
-                }
-            }
+            // passes of J * kThreads elements; in all but the last every
+            // thread has J of them
+            const int full_end = ne - ne % (J * kThreads);
+            for (int base = 0; base < full_end; base += J * kThreads)
+                unaligned_pass<E, OUT, J, true>(p, smem, ringoff, rowptr, shift, wslot, n, c, ne, first,
+                                                base + (int)threadIdx.x);
+            if (full_end < ne)
+                unaligned_pass<E, OUT, J, false>(p, smem, ringoff, rowptr, shift, wslot, n, c, ne, first,
+                                                 full_end + (int)threadIdx.x);
             if constexpr (OUT == kOutAllSgd) {
                 // generic-proxy writes of the new weights -> visible to the bulk copy
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
