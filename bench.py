@@ -254,13 +254,7 @@ def run_reference(args):
     plan = None
     if wl.bucket_cap_bytes:
         # the workload's reverse-order buckets over the first p elements
-        numel, left = [], p
-        for t in wl.tensors:
-            if left <= 0:
-                break
-            numel.append(min(t, left))
-            left -= numel[-1]
-        plan = oracle.bucket_plan(numel, esz, wl.bucket_cap_bytes)
+        plan = oracle.bucket_plan(tensors_within(wl.tensors, p), esz, wl.bucket_cap_bytes)
     for _ in range(args.warmup):
         _oracle_step(wl, rows, w, plan)
     times = []
@@ -671,6 +665,18 @@ def call_bytes(call: str, n: int, p: int, esz: int) -> int:
     raise ValueError(call)
 
 
+def tensors_within(numel, p):
+    """The leading layer tensors that fit p elements (the last one cut), so
+    that a bucket plan over them stays inside rows of p elements."""
+    out, left = [], p
+    for t in numel:
+        if left <= 0:
+            break
+        out.append(min(int(t), left))
+        left -= out[-1]
+    return out
+
+
 def run_profile_call(args):
     """Device-only timing of one entry point on one workload (the launch
     configuration profiled under ncu); inputs from a seeded torch generator
@@ -711,10 +717,10 @@ def run_profile_call(args):
         w = torch.randn(p, generator=g, device="cuda")
         step = lambda: ra.ra_allreduce_sgd(rows, w, wl.sgd_lr or 0.1, stream)
     elif c == "buckets":
-        plan = ra.ra_bucket_plan(wl.tensors, esz, wl.bucket_cap_bytes or 25 * 1024 * 1024)
+        plan = ra.ra_bucket_plan(tensors_within(wl.tensors or (p,), p), esz, wl.bucket_cap_bytes or 25 * 1024 * 1024)
         step = lambda: ra.ra_allreduce_avg_buckets(rows, plan, stream)
     elif c == "buckets_each":  # one call, and so one launch, per bucket
-        plan = ra.ra_bucket_plan(wl.tensors, esz, wl.bucket_cap_bytes or 25 * 1024 * 1024)
+        plan = ra.ra_bucket_plan(tensors_within(wl.tensors or (p,), p), esz, wl.bucket_cap_bytes or 25 * 1024 * 1024)
 
         def step():
             for b in plan:

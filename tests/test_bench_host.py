@@ -52,3 +52,14 @@ def test_call_bytes():
     assert bench.call_bytes("reduce_scatter", n, p, 4) == (n + 1) * p * 4
     assert bench.call_bytes("all_gather", n, p, 4) == n * p * 4
     assert bench.call_bytes("staged", n, p, 4) == 44_400_000_000  # (5(N-1)+2) P s
+
+
+def test_bucket_tensors_cut_to_the_rows():
+    # a reduced --elements run plans buckets only over the tensors that fit,
+    # so that no bucket reaches past the rows it is given
+    wl = synth.WORKLOADS["transformer24_buckets_n4_f32"]
+    for p in (1, 65_536_000, 100_000_000, wl.p):
+        t = bench.tensors_within(wl.tensors, p)
+        assert sum(t) == p and all(x > 0 for x in t)
+        assert t[:-1] == list(wl.tensors[:len(t) - 1])
+    assert bench.tensors_within(wl.tensors, wl.p) == list(wl.tensors)
