@@ -63,3 +63,32 @@ def test_bucket_tensors_cut_to_the_rows():
         assert sum(t) == p and all(x > 0 for x in t)
         assert t[:-1] == list(wl.tensors[:len(t) - 1])
     assert bench.tensors_within(wl.tensors, wl.p) == list(wl.tensors)
+
+
+def test_result_check_finds_any_wrong_element():
+    # bench.py's check of the call it timed: worker 0's row against the
+    # oracle's result on every element, the other workers against worker 0,
+    # the SGD weights against theirs.  Host tensors stand in for device rows.
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(5)
+    for bf16 in (False, True):
+        p = 1000
+        mean = rng.standard_normal(p).astype(np.float32)
+        if bf16:
+            mean = (mean.view(np.uint32) >> 16).astype(np.uint16)
+            rows = [torch.from_numpy(mean.view(np.int16).copy()).view(torch.bfloat16) for _ in range(3)]
+        else:
+            rows = [torch.from_numpy(mean.copy()) for _ in range(3)]
+        w = torch.from_numpy(rng.standard_normal(p).astype(np.float32))
+        wexp = w.numpy().copy()
+        assert bench.check_result(rows, mean, w, wexp, slice_elems=256) == {"bit_exact": True, "first_mismatch": None}
+        bits = torch.int16 if bf16 else torch.int32
+        for who, idx in ((0, 777), (2, 3)):  # one flipped low bit in worker 0, then in worker 2
+            rows[who].view(bits)[idx] ^= 1
+            r = bench.check_result(rows, mean, w, wexp, slice_elems=256)
+            assert r["bit_exact"] is False and str(who if who else idx) in r["first_mismatch"], r
+            rows[who].view(bits)[idx] ^= 1
+        w.view(torch.int32)[999] ^= 1
+        r = bench.check_result(rows, mean, w, wexp, slice_elems=256)
+        assert r["bit_exact"] is False and r["first_mismatch"] == "weights, element 999"
