@@ -15,6 +15,12 @@ replicas' bytes over the slowest replica's time.
 
 --impl reference times the CPU oracle (a literal, single-threaded
 simulation of the ring) on a bounded sample of the same workload.
+
+The CPU leg is the only part of this file that runs the oracle: it times it
+on a bounded sample (cpu_baseline, and the reference arm), and it computes
+the result each verified call must produce, from host copies of that call's
+inputs (fill_workload with verify, then check_result).  The GPU path never
+reads anything the oracle produced.
 """
 from __future__ import annotations
 

@@ -1,8 +1,10 @@
 """CPU oracle for the ring all-reduce -- TEST INFRASTRUCTURE ONLY.
 
-Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this package.  The product library never imports or
-links it, and it shares no code with the CUDA path.
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU leg of
+``bench.py`` (its timed CPU baseline, and its check of the GPU's result
+against host copies of the same inputs) may import this package.  The
+product library never imports or links it, and it shares no code with the
+CUDA path.
 
 This module is a thin ctypes wrapper around ``ring_oracle.c`` (a plain,
 single-threaded C simulation of the ring's scatter-reduce, average and

@@ -3,8 +3,10 @@
  *
  * A plain, slow, single-threaded CPU simulation of the ring all-reduce used for
  * data-parallel gradient averaging.  Only the tests, the smoke check and the
- * CPU-baseline leg of the benchmark may load this file's library; the product
- * path (the CUDA library) never calls it and shares no code with it.
+ * CPU leg of the benchmark (its timed CPU baseline, and its check of the
+ * GPU's result against host copies of the same inputs) may load this file's
+ * library; the product path (the CUDA library) never calls it and shares no
+ * code with it.
  *
  * Sources (page title, section):
  *   [G]  "Andrew Gibiansky: Bringing HPC Techniques to Deep Learning"
