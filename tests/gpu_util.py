@@ -2,8 +2,6 @@
 the layouts the tests need, and read sampled outputs back."""
 from __future__ import annotations
 
-import os
-
 import numpy as np
 import torch
 
@@ -83,49 +81,18 @@ def gather(rows, idx):
     return [to_host(r.index_select(0, it)) for r in rows]
 
 
-def fill_and_expect(wl, rows, rings=None, slice_elems=1 << 24, sub_elems=1 << 15, threads=None):
+def fill_and_expect(wl, rows, rings=None):
     """Put the workload's inputs in `rows` and compute the ring's result for
-    every element on the host.
-
-    The rows are generated slice by slice into a host buffer; each slice is
-    copied to the device rows (tensors of any placement) and, from the same
-    host bytes, the oracle's range evaluation gives the ring's result for
-    every element of the slice.  rings: [(offset, count)] element ranges
-    that are rings of their own (the buckets), or None for one ring over all
-    p elements.  Returns the expected result, p elements (float32, or uint16
-    bf16 bits).  The oracle's calls run on a thread pool (they release the
-    interpreter lock), one sub-slice each."""
-    from concurrent.futures import ThreadPoolExecutor
-
-    import oracle
-
-    n, p = wl.n, wl.p
-    bf16 = wl.dtype == "bf16"
-    hdt = np.uint16 if bf16 else np.float32
-    s_el = min(slice_elems, max(1, p))
-    host = torch.empty((n, s_el), dtype=torch.int16 if bf16 else torch.float32).pin_memory()
-    hnp = host.numpy().view(hdt)
-    expected = np.empty(p, hdt)
-    rings = [(0, p)] if rings is None else list(rings)
-    threads = threads or max(1, min(32, os.cpu_count() or 1))
-    with ThreadPoolExecutor(threads) as ex:
-        for off, cnt in rings:
-            for s in range(0, cnt, s_el):
-                c = min(s_el, cnt - s)
-                for k in range(n):
-                    wl.fill_row(host[k].data_ptr(), k, off + s, c)
-                    src = host[k, :c].view(torch.bfloat16) if bf16 else host[k, :c]
-                    rows[k][off + s:off + s + c].copy_(src, non_blocking=True)
-
-                def part(a, s=s, c=c, off=off, cnt=cnt):
-                    b = min(c, a + sub_elems)
-                    oracle.ring_avg_range([hnp[k, a:b] for k in range(n)], cnt, s + a,
-                                          out=expected[off + s + a:off + s + b])
-
-                list(ex.map(part, range(0, c, sub_elems)))
-                torch.cuda.current_stream().synchronize()  # the copies are done with the host slice
-    del host
-    return expected
+    every element on the host: the rows are generated slice by slice, each
+    slice goes to the device rows and, from the same host bytes, the oracle's
+    range evaluation gives the ring's result for it (bench.fill_workload,
+    which the benchmark uses to check the calls it times).  rings:
+    [(offset, count)] element ranges that are rings of their own (the
+    buckets), or None for one ring over all p elements.  Returns the expected
+    result, p elements (float32, or uint16 bf16 bits)."""
+    import bench
+    mean, _ = bench.fill_workload(wl, rows, None, rings, verify=True)
+    return mean
 
 
 def assert_row_equals(row, expected, begin=0, end=None, what="", slice_elems=1 << 26):
