@@ -429,6 +429,28 @@ PER_CONFIG = (("ring4_uneven_1m_f32", "allreduce"), ("transformer24_buckets_n4_f
               ("resnet18_sgd_n32_f32", "sgd"))
 
 
+def graph_rate(ra, rows, nbytes, peak, calls=100, replays=10):
+    """The same all-reduce captured `calls` times in one CUDA graph and
+    replayed: the GPU's own time per call, without the host's per-call cost
+    (which bounds a call this small when it is issued from Python)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ra.ra_allreduce_avg(rows, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            ra.ra_allreduce_avg(rows, torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    ms, _ = timed_region(lambda k: g.replay(), replays, None, _CudaEventTimer(torch.cuda.current_stream()))
+    per = ms / replays / calls
+    gbs = nbytes / (per / 1e3) / 1e9
+    return {"calls_per_graph": calls, "replays": replays, "ms_per_call": per, "gbs": gbs, "frac": gbs / peak}
+
+
 def measure_config(ra, wl, calls, steps, warmup, peak):
     """One workload, one or more calls on it: verified first call, then
     `warmup` more and `steps` timed.  Returns one result dict per call."""
@@ -469,9 +491,10 @@ def measure_config(ra, wl, calls, steps, warmup, peak):
         k_steps = max(steps, 200) if small else steps
         ms, _ = timed_region(lambda k: step(), k_steps, None, _CudaEventTimer(stream))
         ms /= k_steps
+        nbytes = call_bytes(call, wl.n, wl.p, esz)
+        graph = graph_rate(ra, rows, nbytes, peak) if small and call == "allreduce" else None
         torch.cuda.synchronize()
         st = ra.ra_check_device_errors()
-        nbytes = call_bytes(call, wl.n, wl.p, esz)
         gbs = nbytes / (ms / 1e3) / 1e9
         res = {"workload": wl.name, "call": call, "workers": wl.n, "elements_per_worker": wl.p, "dtype": wl.dtype,
                "bytes_per_call": nbytes, "ms_per_call": ms, "gbs": gbs, "frac": gbs / peak,
@@ -483,8 +506,11 @@ def measure_config(ra, wl, calls, steps, warmup, peak):
         if plan:
             res["buckets"] = len(plan)
             res["launches_per_call"] = len(plan) if call == "buckets_each" else 1
-        if wl.n * wl.p * esz < 129e6:
-            res["note"] = "inputs of %.1f MB fit the 129 MB L2; the call is launch-bound" % (wl.n * wl.p * esz / 1e6)
+        if small:
+            res["note"] = ("inputs of %.1f MB fit the 129 MB L2; issued from Python the call is bound by the host's "
+                           "per-call cost (cuda_graph: the same calls replayed from a graph)" % (wl.n * wl.p * esz / 1e6))
+        if graph:
+            res["cuda_graph"] = graph
         out.append(res)
     del rows, w, keep
     torch.cuda.empty_cache()
