@@ -283,3 +283,50 @@ def test_many_buckets_split_over_launches():
     ra.ra_allreduce_avg_buckets(rows, plan)
     torch.cuda.synchronize()
     _assert_rows_equal_oracle(rows, rows_o[0])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("extra", [-1, 0, 1])
+def test_unaligned_pass_boundaries(dtype, extra):
+    # Rows that disagree modulo 16 bytes take the unaligned kernel, which
+    # runs a tile's passes of J x 256 elements without bounds checks and
+    # checks only the last one.  The chunk lengths here put a tile's element
+    # count exactly on a pass boundary, and one element either side, for
+    # the all-reduce and SGD (J = 2: 512-element passes) and the
+    # reduce-scatter (J = 4: 1024-element passes); a chunk's first and last
+    # 16 bytes go element by element, so the kernel's part is L - 2V.
+    n = 4
+    esz = 4 if dtype == "f32" else 2
+    V = 16 // esz
+    for k in (1, 2, 3, 4, 5, 8, 9):
+        L = 2 * V + 512 * k + extra
+        p = n * L
+        host = _host_rows(n, p, dtype, seed=50 + k)
+        want = _oracle(host, dtype)
+        rows = to_device_rows(host, layout="mixed", pad=1)
+        ra.ra_allreduce_avg(rows)
+        torch.cuda.synchronize()
+        _assert_rows_equal_oracle(rows, want)
+
+        # SGD on the same rows, weights offset by one element
+        rows = to_device_rows(host, layout="mixed", pad=1)
+        w0 = synth.normal_f32(60 + k, 0, 0.05, 0, p)
+        wbase = torch.empty(p + 4, dtype=torch.float32, device="cuda")
+        w = wbase[1:1 + p]
+        w.copy_(torch.from_numpy(w0))
+        ra.ra_allreduce_sgd(rows, w, 0.1)
+        torch.cuda.synchronize()
+        _assert_rows_equal_oracle(rows, want)
+        wexp = w0.copy()
+        oracle.sgd_update_f32(wexp, want, np.float32(0.1))
+        np.testing.assert_array_equal(w.cpu().numpy().view(np.uint32), wexp.view(np.uint32))
+
+        # reduce-scatter: each chunk's mean on the worker that owns it
+        rows = to_device_rows(host, layout="mixed", pad=1)
+        ra.ra_reduce_scatter_avg(rows)
+        torch.cuda.synchronize()
+        owned = oracle.reduce_scatter_avg([h.copy() for h in host])
+        for wk, (b, e) in owned.items():
+            got = to_host(rows[wk])[b:e]
+            bits = np.uint32 if dtype == "f32" else np.uint16
+            np.testing.assert_array_equal(got.view(bits), want[b:e].view(bits), err_msg="k=%d worker %d" % (k, wk))
