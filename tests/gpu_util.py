@@ -1,11 +1,10 @@
 """Helpers for the GPU parity tests: put seeded host rows on the device in
-the layouts the tests need, and read sampled outputs back."""
+the layouts the tests need, fill full-size workloads with the oracle's
+expected result beside them, and compare device rows with it."""
 from __future__ import annotations
 
 import numpy as np
 import torch
-
-import synth
 
 
 def to_device_rows(host_rows, layout="separate", pad=0):
@@ -61,24 +60,6 @@ def sample_indices(p, n, rng, count=2000, extra=()):
         if 0 <= i < p:
             idx.add(i)
     return np.array(sorted(idx), dtype=np.int64)
-
-
-def fill_device_rows(wl, rows, chunk_elems=1 << 26):
-    """Generate workload rows on the host in pieces and copy them to `rows`."""
-    p = wl.p
-    bf16 = wl.dtype == "bf16"
-    host = torch.empty(min(p, chunk_elems), dtype=torch.int16 if bf16 else torch.float32).pin_memory()
-    for k, r in enumerate(rows):
-        for s in range(0, p, chunk_elems):
-            cnt = min(chunk_elems, p - s)
-            wl.fill_row(host.data_ptr(), k, s, cnt)
-            src = host[:cnt].view(torch.bfloat16) if bf16 else host[:cnt]
-            r[s:s + cnt].copy_(src, non_blocking=False)
-
-
-def gather(rows, idx):
-    it = torch.from_numpy(idx).to("cuda")
-    return [to_host(r.index_select(0, it)) for r in rows]
 
 
 def fill_and_expect(wl, rows, rings=None):

@@ -14,7 +14,7 @@ import torch
 import gradient_ring_all_gb300 as ra
 import oracle
 import synth
-from gpu_util import fill_device_rows, gather, sample_indices, to_device_rows, to_host
+from gpu_util import to_device_rows, to_host
 
 pytestmark = pytest.mark.gpu
 
