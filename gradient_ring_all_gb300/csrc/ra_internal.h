@@ -154,8 +154,6 @@ __host__ __device__ inline void unaligned_interior(int64_t b, int64_t e, int V, 
 // (room for the widening), a weight slot for SGD, the mbarrier, the per-row
 // byte offsets and staging offsets, and (8-byte aligned) the rows' tile
 // pointers
-// n row slots | weight slot (SGD) | mbarrier | shift[n + 1], ringoff[n] |
-// (8-byte alignment) rowptr[n]
 inline size_t unaligned_smem_bytes(int n, int tile_bytes, int out, int esz) {
     return (size_t)n * ((size_t)tile_bytes + 16) + (out == kOutAllSgd ? (size_t)(tile_bytes / esz) * 4 + 16 : 0) + 16 +
            (size_t)(2 * n + 1) * sizeof(int) + 8 + (size_t)n * sizeof(char *);
@@ -211,9 +209,11 @@ struct GatherLaunch {
 cudaError_t launch_all_gather(const GatherLaunch &L, cudaStream_t s);
 
 // bytes of the owner's chunk one block of the TMA all-gather stages at a
-// time (measured on GB300, N=8 f32: 16 KB 6.78, 32 KB 6.85, 64 KB 6.89 TB/s)
+// time: one block per SM at this size (measured on GB300, N=8 f32: 16 KB
+// 6.78, 32 KB 6.85, 64 KB 6.88-6.89, 96 KB 6.91, 128 KB 7.02, 192 KB 7.01-
+// 7.02 TB/s; bf16 N=16 and f32 N=4 gain the same 1.7 % from 64 to 128 KB)
 #ifndef RA_GATHER_TILE_BYTES
-#define RA_GATHER_TILE_BYTES 65536
+#define RA_GATHER_TILE_BYTES 131072
 #endif
 constexpr int kGatherTileBytes = RA_GATHER_TILE_BYTES;
 
