@@ -470,12 +470,16 @@ __global__ void __launch_bounds__(kThreads) fused_tma_kernel(const __grid_consta
 //          boundaries (first byte rounded down, end rounded up) into a slot
 //          of B + 16 bytes; the row's elements start d_k bytes into the slot.
 //   fold:  each thread takes J elements of the tile and walks the rows in
-//          ring order, reading every row at its own offset, so the per-row
-//          work (offset, address) is shared by J elements.
+//          ring order through a table thread 0 writes per tile (where row
+//          (c + t) mod n starts in shared memory), reading every row at its
+//          own offset, so the per-row work is shared by J elements; every
+//          pass but the tile's last runs without bounds checks.
 //   store: the mean leaves by scalar stores, coalesced across the warp, as
 //          soon as it is known.  (Writing it back into shared memory first
-//          and storing whole 16-byte granules -- by bulk copies or by
-//          16-byte thread stores -- measured slower on GB300.)
+//          and storing whole 16-byte granules -- by bulk copies, from one
+//          slot per distinct row offset, or by 16-byte thread stores --
+//          measured slower on GB300: the block barrier they need holds the
+//          staging longer.)
 // The SGD weights are one more widened bulk copy in and, for their whole
 // granules, a bulk copy out.  Tiles keep 16 bytes away from both ends of
 // their segment (those elements take the scalar path), so the widened copies
