@@ -92,3 +92,15 @@ def test_result_check_finds_any_wrong_element():
         w.view(torch.int32)[999] ^= 1
         r = bench.check_result(rows, mean, w, wexp, slice_elems=256)
         assert r["bit_exact"] is False and r["first_mismatch"] == "weights, element 999"
+
+
+def test_per_config_covers_every_other_workload():
+    # the recorded benchmark line measures and verifies every configuration:
+    # the headline, plus each other workload (the bucketed one both ways)
+    names = {w for w, _ in bench.PER_CONFIG}
+    assert names | {bench.WORKLOAD} == set(synth.WORKLOADS)
+    assert ("transformer24_buckets_n4_f32", "buckets") in bench.PER_CONFIG
+    assert ("transformer24_buckets_n4_f32", "buckets_each") in bench.PER_CONFIG
+    assert ("resnet18_sgd_n32_f32", "sgd") in bench.PER_CONFIG
+    for _, call in bench.PER_CONFIG:
+        assert call in bench.CALLS
